@@ -1,0 +1,429 @@
+"""Benchmark of the ZeRO shard step on GB300: parameters updated per second and achieved
+HBM bandwidth against the measured peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch of synthetic input: the
+rank-order sum of the Nd fp16 gradient contributions, the overflow flag and exact norm,
+and the clipped AdamW update with the fp16 cast (two kernels). The default workload is
+the GPT-2-small-sized flat buffer (N = 124,439,808, Nd = 8, 128-element alignment, clip
+1.0). Inputs (2 GB of gradients per step, two alternating sets) are larger than L2, so no
+flush is needed between steps.
+
+For N > 1 (launched with torch.distributed.run, one process per GPU) GPU g owns the
+logical ranks [g*Nd/N, (g+1)*Nd/N) of the same model (strong scaling); the one exchange
+step is an NCCL all-reduce of the 64-byte statistics buffer between the two halves of
+the step.
+
+``--impl reference`` times the CPU oracle (single-threaded C) on a bounded sample of the
+same workload instead; it needs no GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO shard-step params/s; achieved HBM GB/s as % of GB300 peak"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+STEP_INFO_D2H_BYTES = 88  # the device scalars block that zero_step_result copies back
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e18)]
+        used = inside or rows[-3:]
+        sm = [float(p[1]) for _, p in used if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in used if p[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in used:
+            for name, val in zip(names, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None,
+               "reasons": sorted(reasons),
+               "samples_in_timed_region": len(inside)}
+        pw = [float(p[3]) for _, p in used if p[3].replace(".", "").isdigit()]
+        if pw:
+            out["power_w_max"] = max(pw)
+        return out
+
+
+# ------------------------------------------------------------------------------------
+# CPU oracle timing (test infrastructure; the only place the bench runs the oracle)
+
+def cpu_sample(w, n):
+    """The first n parameters of the workload's span, generated on the CPU by the seeded
+    generator: two gradient sets and the initial master/m/v/param16."""
+    import numpy as np
+
+    import synth
+    from synth import workloads as wl
+    first = w.span()[0]
+    master = synth.values_f32(wl.key(w, synth.MASTER), w.master_sigma, first, n)
+    m = (synth.values_f32(wl.key(w, synth.EXP_AVG), w.m_sigma, first, n) if w.m_sigma > 0
+         else np.zeros(n, np.float32))
+    v = (synth.values_f32(wl.key(w, synth.EXP_AVG_SQ), w.v_sigma, first, n, absolute=True)
+         if w.v_sigma > 0 else np.zeros(n, np.float32))
+    p16 = master.astype(np.float16).view(np.uint16).copy()
+    grads = [[synth.values_f16(wl.key(w, synth.GRAD, st, k), w.grad_sigma * w.loss_scale,
+                               first, n) for k in range(w.nd)] for st in range(2)]
+    return grads, master, m, v, p16
+
+
+def oracle_steps(w, n, steps=None, seconds=None, warmup=0):
+    """Run the single-threaded oracle on a CPU sample of n parameters, either a fixed
+    number of steps or until ``seconds`` pass. Returns (params/s, steps, seconds)."""
+    import oracle
+    grads, master, m, v, p16 = cpu_sample(w, n)
+    hp = oracle.Hyper(**w.hparams())
+    t = 0
+    for i in range(warmup):
+        t = oracle.step(grads[i % 2], master, m, v, p16, w.loss_scale, w.clip, hp, t).step
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        t = oracle.step(grads[done % 2], master, m, v, p16, w.loss_scale, w.clip, hp, t).step
+        done += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and done >= steps) or (seconds is not None and el >= seconds):
+            break
+    return n * done / el, done, el
+
+
+def sample_size(w, max_params):
+    n = min(max_params, w.span()[2])
+    return max(8, n - n % 8)
+
+
+def oracle_sample_rate(w, seconds: float, max_params: int = 4_000_000):
+    n = sample_size(w, max_params)
+    rate, steps, el = oracle_steps(w, n, seconds=seconds)
+    desc = (f"oracle.step (single-threaded C, -O2) on the first {n:,} parameters of the "
+            f"span, {steps} steps in {el:.1f} s; norm and clip taken over the sample")
+    return rate, desc
+
+
+def run_reference(args, w):
+    rank = env_int("RANK", 0)
+    if rank != 0:
+        return 0
+    # size one step's sample so that warmup + steps take about two minutes at most
+    rate0, _, _ = oracle_steps(w, sample_size(w, 65536), seconds=0.5)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    n = sample_size(w, int(max(8192, min(4_000_000, rate0 * per_step))))
+    value, _, el = oracle_steps(w, n, steps=args.steps, warmup=args.warmup)
+    sample = (f"oracle.step (single-threaded C) on the first {n:,} of {w.span()[2]:,} "
+              f"parameters per step; norm and clip over the sample")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(w, n_gpus):
+    first, n_span, n_valid = w.span()
+    return {"workload": w.name, "n_params": w.n, "nd": w.nd, "align": w.align,
+            "stage": w.stage, "span_ranks": [w.r0, w.r1], "params_in_span": n_valid,
+            "loss_scale": w.loss_scale, "clip": w.clip,
+            "parallelism": f"zero{w.stage} nd{w.nd} on {n_gpus} gpu",
+            "l2": "inputs larger than L2 (two alternating gradient sets of "
+                  f"{2 * w.nd * n_span / 1e9:.2f} GB each); no flush",
+            "io": "fp16 grads in, fp32 master/m/v, fp16 params out"}
+
+
+# ------------------------------------------------------------------------------------
+
+def run_ours(args, w0):
+    import torch
+
+    import sharded_emulated_reduce_gb300 as z
+    from synth import workloads as wl
+
+    world = env_int("WORLD_SIZE", 1)
+    rank = env_int("RANK", 0)
+    local = env_int("LOCAL_RANK", 0)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    if w0.nd % world:
+        raise SystemExit(f"--gpus {world} must divide Nd = {w0.nd}")
+    per = w0.nd // world
+    w = dataclasses.replace(w0, r0=rank * per, r1=(rank + 1) * per)
+    first, n_span, n_valid = w.span()
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    master, m, v, p16, ws = wl.make_state(w, dev)
+    gsets = [wl.make_grads(w, s, dev) for s in range(2)]
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, w.r0, w.r1, master, m, v, p16, ws, 0)
+    stream = torch.cuda.current_stream()
+    stats_t = None
+    if dist is not None:
+        stats_t = torch.zeros(z.ZERO_STATS_WORDS, dtype=torch.int64, device=dev)
+        stats_addr = z.zero_shard_stats(plan)
+
+    def one_step(grads):
+        if dist is None:
+            z.zero_shard_step(plan, w.r0, w.r1, grads, w.loss_scale, w.clip, stream)
+        else:
+            z.zero_shard_reduce(plan, w.r0, w.r1, grads, stream)
+            # exchange: sum the statistics words of all ranks (exact integers)
+            copy_words(stats_addr, stats_t, to_tensor=True)
+            dist.all_reduce(stats_t)
+            copy_words(stats_addr, stats_t, to_tensor=False)
+            z.zero_shard_update(plan, w.r0, w.r1, w.loss_scale, w.clip, stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        one_step(gsets[i % 2])
+    barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    z.zero_profile_read(plan, reset=True)
+    z.zero_profile_enable(plan, True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark("start")
+    e0.record(stream)
+    for i in range(args.steps):
+        one_step(gsets[i % 2])
+    e1.record(stream)
+    barrier()
+    clocks.mark("end")
+    ms_total = e0.elapsed_time(e1)
+    z.zero_profile_enable(plan, False)
+    kms, klaunch = z.zero_profile_read(plan, reset=True)
+    clk = clocks.stop()
+    info = z.zero_step_result(plan).as_dict()
+
+    ms = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    ms_per_step = ms.item() / args.steps
+    total_params = w0.span()[2]
+    value = total_params / (ms_per_step / 1e3)
+
+    # e2e through the public API with host buffers: per step the H2D copy of the step's
+    # gradients from pinned host memory, the step, and the D2H read of its result
+    host = [[g.cpu().pin_memory() for g in gs] for gs in gsets]
+    dev_g = [torch.empty_like(g) for g in gsets[0]]
+    e2e_steps = max(3, min(args.steps, 100))
+    for i in range(2):
+        for d, h in zip(dev_g, host[i % 2]):
+            d.copy_(h, non_blocking=True)
+        one_step(dev_g)
+        z.zero_step_result(plan)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        for d, h in zip(dev_g, host[i % 2]):
+            d.copy_(h, non_blocking=True)
+        one_step(dev_g)
+        z.zero_step_result(plan)
+    barrier()
+    e2e_s = torch.tensor([(time.perf_counter() - t0) / e2e_steps], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(e2e_s, op=dist.ReduceOp.MAX)
+    e2e_value = total_params / e2e_s.item()
+    h2d = sum(g.numel() * g.element_size() for g in gsets[0]) * world
+
+    peak, peak_kind = load_peaks()
+    n_real = n_valid
+    kinds = {0: ("reduce", (2 * w.nd + 4) * n_span),
+             1: ("update", 30 * n_real),
+             2: ("finalize", 0)}
+    dom = max((k for k in kinds if klaunch[k]), key=lambda k: kms[k])
+    name, alg_bytes = kinds[dom]
+    avg_ms = kms[dom] / klaunch[dom]
+    achieved = alg_bytes / (avg_ms / 1e3) / 1e9
+    traffic = load_traffic(name, w)
+    roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
+                "avg_launch_ms": avg_ms,
+                "time_share": {kinds[k][0]: kms[k] / sum(kms[:3]) for k in kinds if klaunch[k]}}
+    step_alg = (2 * w0.nd + 26) * total_params
+    step_gbs = step_alg / (ms_per_step / 1e3) / 1e9
+    moved = (2 * w0.nd + 34) * total_params / (ms_per_step / 1e3) / 1e9
+
+    if rank != 0:
+        return 0
+    rate, desc = oracle_sample_rate(w0, args.cpu_seconds) if args.cpu_seconds > 0 \
+        else (None, "skipped")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(w0, world),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": STEP_INFO_D2H_BYTES * world, "steps": e2e_steps},
+        "gpu_launches": int(sum(klaunch[:3])) * world,
+        "roofline": roofline,
+        "step_hbm": {"alg_bytes_per_param": 2 * w0.nd + 26, "alg_gbs": step_gbs,
+                     "alg_frac": step_gbs / peak,
+                     "min_moved_bytes_per_param": 2 * w0.nd + 34, "min_moved_gbs": moved,
+                     "min_moved_frac": moved / peak, "peak": peak, "peak_kind": peak_kind},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "clocks": clk,
+        "last_step": {k: info[k] for k in ("step", "skipped", "global_norm", "clip_coef")},
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    plan.close()
+    return 0
+
+
+def copy_words(addr, tensor, to_tensor: bool):
+    """Device-to-device copy between the plan's statistics words and a torch tensor."""
+    import ctypes
+
+    import torch
+    cudart = ctypes.CDLL("libcudart.so.13")
+    n = tensor.numel() * 8
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    dst, src = (tensor.data_ptr(), addr) if to_tensor else (addr, tensor.data_ptr())
+    rc = cudart.cudaMemcpyAsync(ctypes.c_void_p(dst), ctypes.c_void_p(src), ctypes.c_size_t(n),
+                                3, stream)  # cudaMemcpyDeviceToDevice
+    if rc != 0:
+        raise RuntimeError(f"cudaMemcpyAsync failed: {rc}")
+
+
+def load_traffic(kernel: str, w):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the same
+    kernel source and workload; None otherwise."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    src = os.path.join(ROOT, "sharded_emulated_reduce_gb300", "csrc", "step_kernels.cu")
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    ent = d.get(w.name, {}).get(kernel)
+    if not ent or ent.get("source_sha256_16") != h:
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def main(argv=None):
+    from synth import workloads as wl
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="gpt2_small_flat_nd8", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU oracle baseline budget (0 skips it)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

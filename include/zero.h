@@ -1,0 +1,201 @@
+/* libzero: the data-parallel hot path of ZeRO (Zero Redundancy Optimizer) on one GB300.
+ *
+ * ZeRO keeps data-parallel training but partitions the model states (optimizer states,
+ * gradients, parameters) across the Nd data-parallel ranks instead of replicating them
+ * ("ZeRO" method entry, codewithpapers.app/method/zero, description; ZeRO explainer,
+ * papermap.vercel.app, "The 16 Bytes per Parameter Audit" and Chapter 02 "The Three
+ * Stages"). This library computes what one device does in that scheme:
+ *
+ *   - the partition of a flat parameter buffer into Nd aligned shards;
+ *   - the shard step: the sum of the Nd ranks' fp16 gradient contributions over the
+ *     owned span (the arithmetic of the reduce-scatter after backward, Chapter 02,
+ *     ZeRO-3 item), the inf/nan overflow check, unscaling by the loss scale, optional
+ *     global-norm clipping, the mixed-precision AdamW update of the fp32 master weights
+ *     and moments, and the fp16 cast (Chapter 02 "Memory per parameter");
+ *   - the ZeRO-3 gather of fp16 shards into contiguous per-layer buffers (the
+ *     arithmetic of the all-gather before forward, Chapter 02, ZeRO-3 item);
+ *   - the per-rank memory accounting of the stage ladder (Chapter 02 "What each stage
+ *     shards" and the stage table after Chapter 05).
+ *
+ * The Nd logical ranks are emulated on one device: their contributions are Nd device
+ * buffers, and no inter-GPU collective is issued. A span of logical ranks [r0, r1) can
+ * be split across processes; zero_shard_reduce / zero_shard_stats / zero_shard_update
+ * expose the single exchange step (a sum of a few integers) for that case.
+ *
+ * Conventions for every call:
+ *   - Device memory (gradients, state, workspace, shards, layer buffers) is allocated
+ *     and owned by the caller; the library never frees it. A plan owns only its host
+ *     metadata, a small device scratch area (< 64 KiB, allocated by zero_plan_bind on
+ *     the device current at that time, freed by zero_plan_destroy) and a few pinned
+ *     host bytes.
+ *   - Element types: fp16 buffers are IEEE binary16 (as torch.float16), fp32 buffers
+ *     are IEEE binary32. All buffers are contiguous 1-D.
+ *   - Streams are cudaStream_t passed as void*; NULL is the legacy default stream.
+ *     Launching calls are asynchronous and return once the work is enqueued.
+ *   - Return codes: ZERO_OK (0) or a negative ZERO_E* code. On any error nothing is
+ *     launched and no state changes; zero_last_error() then gives a message.
+ *   - An overflow (inf/nan among the summed gradients) is not an error: the step is
+ *     skipped on the device and zero_step_result reports it.
+ *   - A plan is not thread-safe; use one plan per host thread.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_OK 0
+#define ZERO_EINVAL (-1)   /* an argument is out of range or inconsistent            */
+#define ZERO_EALIGN (-2)   /* a device pointer is not 16-byte aligned                */
+#define ZERO_EUNBOUND (-3) /* the plan has no state bound for the requested span     */
+#define ZERO_ECUDA (-4)    /* a CUDA runtime call failed                             */
+#define ZERO_EDEVICE (-5)  /* a kernel reported a failure status (see step info)     */
+
+#define ZERO_MAX_ND 256        /* largest supported number of logical ranks Nd         */
+#define ZERO_STATS_WORDS 8     /* int64 words in the exchange buffer of zero_shard_stats */
+
+/* AdamW hyperparameters (fp32). */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+} zero_adam_hparams;
+
+/* Result of the last step of a plan. */
+typedef struct {
+  int32_t overflow;   /* 1 if any summed gradient in the span was inf or nan          */
+  int32_t skipped;    /* 1 if the update was not applied (overflow or status != 0)    */
+  int32_t status;     /* 0, or a device-side failure code (nothing was written)       */
+  int32_t reserved;
+  int64_t step;       /* optimizer step counter after the step                        */
+  double global_norm; /* L2 norm of the unscaled summed gradient (+inf on overflow)   */
+  double sum_sq;      /* exact sum of squares of the scaled summed gradient, rounded   */
+  double clip_coef;   /* min(1, clip / (global_norm + 1e-6)), or 1 without clipping    */
+  float scale;        /* fp32 factor applied to the summed gradient: clip_coef / loss_scale */
+  float bc1, bc2;     /* fp32 bias corrections 1 - beta^step used by the update       */
+  float reserved2;
+} zero_step_info;
+
+typedef struct zero_plan zero_plan; /* opaque */
+
+/* Create a plan for a flat buffer of n_params parameters partitioned over nd ranks.
+ * Partition ("ZeRO" method entry, description: partition the model states): the buffer
+ * is padded to Np = ceil(n_params / (nd * align)) * nd * align elements and shard r is
+ * [r*S, (r+1)*S) with S = Np / nd; the shards concatenate exactly to the padded buffer,
+ * and the padding [n_params, Np) holds no parameter.
+ *   n_params >= 1; 1 <= nd <= ZERO_MAX_ND; stage in {1, 2, 3} (ZeRO-1/2/3: which state
+ *   classes are partitioned; the step's arithmetic is the same for all three);
+ *   align >= 8 and a multiple of 8 (elements); Np * nd^2 < 2^47 (keeps the exact sum of
+ *   squares within 128 bits); hp non-NULL with 0 <= beta1, beta2 < 1, lr >= 0, eps > 0,
+ *   weight_decay >= 0, all finite.
+ * On success *out receives a new plan (free it with zero_plan_destroy). Host only: no
+ * CUDA call is made. Errors: ZERO_EINVAL. */
+int zero_plan_create(int64_t n_params, int32_t nd, int32_t stage, int32_t align,
+                     const zero_adam_hparams* hp, zero_plan** out);
+
+/* Free a plan and its device scratch. NULL is ignored. The caller's buffers are not
+ * touched. Any work enqueued with the plan must have completed. */
+void zero_plan_destroy(zero_plan* plan);
+
+/* The plan's padded length Np and shard length S (shard r starts at r * S). */
+int zero_plan_layout(const zero_plan* plan, int64_t* padded_len, int64_t* shard_len);
+
+/* Bytes of fp32 workspace the step needs for the span of logical ranks [r0, r1):
+ * 4 * (r1 - r0) * S. Returns the byte count, or a negative ZERO_E* code. */
+int64_t zero_workspace_bytes(const zero_plan* plan, int32_t r0, int32_t r1);
+
+/* Bind the optimizer state of the span [r0, r1) (0 <= r0 < r1 <= nd; n = (r1-r0)*S
+ * elements, element i is flat index r0*S + i):
+ *   master, exp_avg, exp_avg_sq: fp32[n], device, read and written by the step;
+ *   param16: fp16[n], device, written by the step (the fp16 parameter copy);
+ *   workspace: zero_workspace_bytes(plan, r0, r1) bytes of device memory, scratch;
+ *   initial_step: the optimizer step counter t before the first step (>= 0).
+ * Every pointer must be non-NULL and 16-byte aligned (ZERO_EALIGN otherwise). Elements
+ * in the padding are never read or written. The first bind allocates the plan's device
+ * scratch on the current device; rebinding replaces the state pointers and resets the
+ * step counter. Synchronous. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float* exp_avg,
+                   float* exp_avg_sq, void* param16, void* workspace, int64_t initial_step);
+
+/* One shard step over the bound span [r0, r1) (must equal the bound span):
+ *   grad_ptrs: host array of nd device pointers; grad_ptrs[k] is rank k's fp16
+ *     gradient for the span, n elements, 16-byte aligned. Element i of every rank
+ *     belongs to flat index r0*S + i.
+ *   loss_scale: finite and > 0; the summed gradient is divided by it.
+ *   clip: global-norm threshold; <= 0 disables clipping. Must be finite.
+ * Computes, on the device, gsum = the fp32 sum of the nd contributions in rank order
+ * 0..nd-1 (the reduce-scatter's arithmetic), the overflow flag and the norm over the
+ * span's real parameters, and, unless the flag is set, the AdamW update of master,
+ * exp_avg and exp_avg_sq with the fp16 cast into param16; the step counter advances
+ * only on an applied step. Enqueued on stream; no host synchronisation. The two kernel
+ * launches it makes contain no host-side decision, so the call can be captured in a
+ * CUDA graph. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EUNBOUND, ZERO_ECUDA. */
+int zero_shard_step(zero_plan* plan, int32_t r0, int32_t r1, const void* const* grad_ptrs,
+                    float loss_scale, float clip, void* stream);
+
+/* First half of zero_shard_step for a span split across processes: the rank-order sum
+ * into the workspace and the span's statistics into the plan's exchange buffer
+ * (zero_shard_stats). Same arguments and errors as zero_shard_step. */
+int zero_shard_reduce(zero_plan* plan, int32_t r0, int32_t r1, const void* const* grad_ptrs,
+                      void* stream);
+
+/* The plan's exchange buffer: ZERO_STATS_WORDS int64 on the device, written by
+ * zero_shard_reduce: word 0 counts non-finite summed gradients, words 1..4 hold the
+ * exact sum of squares of (gsum * 2^24) as four 32-bit limbs (least significant first),
+ * words 5..7 are zero. Summing the buffers of all processes word by word (an integer
+ * all-reduce) gives the statistics of the whole buffer. Valid after zero_plan_bind. */
+int zero_shard_stats(zero_plan* plan, void** dev_words);
+
+/* Second half of zero_shard_step: reads the (possibly all-reduced) exchange buffer,
+ * decides skip, norm and clip coefficient, and applies the update to the bound span.
+ * Errors as zero_shard_step. */
+int zero_shard_update(zero_plan* plan, int32_t r0, int32_t r1, float loss_scale, float clip,
+                      void* stream);
+
+/* Wait for the plan's last step to finish and copy its result to *out. This is the
+ * only call that synchronises with the device. Errors: ZERO_EINVAL, ZERO_EUNBOUND (no
+ * step yet), ZERO_ECUDA, ZERO_EDEVICE (out is still filled). */
+int zero_step_result(zero_plan* plan, zero_step_info* out);
+
+/* ZeRO-3 gather ("all-gather before forward", ZeRO explainer, Chapter 02): with flat =
+ * the concatenation of the nd fp16 shards of S elements each, copies
+ * layer_dst[l][j] = flat[layer_offsets[l] + j] for 0 <= j < layer_offsets[l+1] -
+ * layer_offsets[l].
+ *   layer_offsets: host int64[n_layers + 1], non-decreasing, 0 <= offsets <= n_params
+ *     (offsets index the unpadded flat buffer);
+ *   shard_ptrs: host array of nd device pointers, fp16[S] each (2-byte aligned);
+ *   layer_dst: host array of n_layers device pointers (2-byte aligned; may be NULL for
+ *     an empty layer). Destinations must not overlap the shards or each other.
+ * For ZeRO-1/2 the parameter all-gather is this call with one layer [0, n_params).
+ * Enqueued on stream. Errors: ZERO_EINVAL, ZERO_ECUDA. */
+int zero_gather_layers(zero_plan* plan, const int64_t* layer_offsets, int32_t n_layers,
+                       const void* const* shard_ptrs, void* const* layer_dst, void* stream);
+
+/* Per-rank model-state bytes (ZeRO explainer, "The 16 Bytes per Parameter Audit",
+ * Chapter 02 and the stage table): 2 B fp16 parameter + 2 B fp16 gradient + 12 B of
+ * optimizer state (fp32 master, momentum, variance) per parameter, with S the padded
+ * shard length of create's partition:
+ *   stage 0 (plain data parallel) 16 N; stage 1 4 N + 12 S; stage 2 2 N + 14 S;
+ *   stage 3 16 S.
+ * Host only. Errors: ZERO_EINVAL. */
+int zero_memory_bytes(int64_t n_params, int32_t nd, int32_t align, int32_t stage,
+                      int64_t* per_rank_bytes);
+
+/* Kernel timing with CUDA events on the launching stream, for profiling. When enabled,
+ * every kernel the plan launches is bracketed by two events; zero_profile_read
+ * synchronises and returns, per kernel kind (0 reduce, 1 update, 2 finalize, 3 gather),
+ * the summed milliseconds and the launch count, then clears them if reset != 0. Off by
+ * default. Errors: ZERO_EINVAL, ZERO_ECUDA. */
+#define ZERO_PROF_KINDS 4
+int zero_profile_enable(zero_plan* plan, int32_t on);
+int zero_profile_read(zero_plan* plan, double* ms, int64_t* launches, int32_t reset);
+
+/* Message of the calling thread's last error ("" if none). Valid until the thread's
+ * next libzero call. */
+const char* zero_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_H */

@@ -1,0 +1,91 @@
+// Internal interface between the host side of libzero (plan.cpp) and its kernels
+// (step_kernels.cu, gather_kernel.cu). Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/zero.h"
+
+namespace zero {
+
+constexpr int kThreads = 256;        // threads per CTA for every kernel
+constexpr int kMaxPartialBlocks = 1024;  // CTAs of the reduce kernel (one partial each)
+constexpr int kGatherSegs = 128;     // copy segments per gather launch
+
+// Scalars of one step, written by the finalize stage and read by the update kernel.
+struct DevScalars {
+  int32_t overflow, skipped, status, pad;
+  int64_t step;  // step counter after this step
+  double ss, norm, clip_coef;
+  float s, omb1, omb2, bc1, bc2, decay, lr, beta1, beta2, eps;
+};
+
+// One reduce CTA's statistics: the 128-bit sum of squares and the non-finite count.
+struct DevPartial {
+  unsigned long long lo, hi;
+  long long bad;
+  long long pad;
+};
+
+// The plan's device scratch (one allocation, < 64 KiB).
+struct DevScratch {
+  long long stats[ZERO_STATS_WORDS];  // exchange buffer (see zero_shard_stats)
+  DevScalars sc;
+  long long step;       // optimizer step counter t
+  unsigned int ticket;  // arrival counter of the reduce CTAs
+  unsigned int pad;
+  DevPartial partials[kMaxPartialBlocks];
+};
+
+struct HostHParams {
+  float lr, beta1, beta2, eps, weight_decay;
+};
+
+struct ReduceLaunch {
+  const void* const* grads;  // host array of nd device pointers (span-relative)
+  int nd;
+  float* gsum;               // workspace, n_span floats
+  int64_t n_span;            // elements in the span (multiple of 8)
+  int64_t n_valid;           // real parameters at the start of the span
+  DevScratch* scratch;
+  bool finalize;             // compute the step scalars in the last CTA
+  float loss_scale, clip;
+  HostHParams hp;
+  int grid;                  // CTAs (<= kMaxPartialBlocks)
+};
+
+struct UpdateLaunch {
+  const float* gsum;
+  float *master, *exp_avg, *exp_avg_sq;
+  void* param16;
+  int64_t n_span, n_valid;
+  DevScratch* scratch;
+  int grid;
+};
+
+struct GatherSeg {
+  const uint16_t* src;
+  uint16_t* dst;
+  int64_t len;         // elements
+  int64_t tile_begin;  // first global tile index of this segment
+};
+
+struct GatherLaunch {
+  GatherSeg seg[kGatherSegs];
+  int nseg;
+  int64_t tiles;       // total tiles over all segments
+  int grid;
+};
+
+constexpr int64_t kGatherTile = 8192;  // elements per gather tile (16 KiB)
+
+cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s);
+cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,
+                            const HostHParams& hp, cudaStream_t s);
+cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s);
+cudaError_t launch_gather(const GatherLaunch& p, cudaStream_t s);
+
+// Occupancy-derived persistent grid size of the gather for the current device.
+int gather_grid(int64_t tiles);
+
+}  // namespace zero

@@ -1,0 +1,527 @@
+// Host side of libzero: plans, argument checks, the gather's segment planner, kernel
+// timing and the C ABI declared in include/zero.h.
+//
+// Every entry point checks all of its arguments before it makes any CUDA call, so an
+// invalid call launches nothing and changes nothing.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using zero::DevScratch;
+
+namespace {
+
+thread_local std::string g_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ZERO_ECUDA, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct EventPair {
+  cudaEvent_t start = nullptr, stop = nullptr;
+  int kind = 0;
+};
+
+constexpr size_t kMaxPendingEvents = 1 << 16;
+
+}  // namespace
+
+struct zero_plan {
+  int64_t n = 0, np = 0, s = 0;
+  int32_t nd = 0, stage = 0, align = 0;
+  zero::HostHParams hp{};
+
+  bool bound = false;
+  int32_t r0 = 0, r1 = 0;
+  float *master = nullptr, *exp_avg = nullptr, *exp_avg_sq = nullptr;
+  void* param16 = nullptr;
+  float* workspace = nullptr;
+
+  int device = -1;
+  DevScratch* scratch = nullptr;
+  zero::DevScalars* host_sc = nullptr;  // pinned
+  cudaStream_t last_stream = nullptr;
+  bool stepped = false;
+
+  bool prof = false;
+  std::vector<EventPair> free_events, pending;
+  double prof_ms[ZERO_PROF_KINDS] = {0, 0, 0, 0};
+  int64_t prof_launches[ZERO_PROF_KINDS] = {0, 0, 0, 0};
+};
+
+namespace {
+
+// Padded length and shard length; written independently of any other module from the
+// definition: pad to a multiple of nd * align, split into nd equal shards.
+void partition(int64_t n, int32_t nd, int32_t align, int64_t* np, int64_t* s) {
+  const int64_t unit = (int64_t)nd * align;
+  *np = (n + unit - 1) / unit * unit;
+  *s = *np / nd;
+}
+
+int check_span(const zero_plan* p, int32_t r0, int32_t r1) {
+  if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+  if (r0 < 0 || r1 > p->nd || r0 >= r1)
+    return fail(ZERO_EINVAL, "rank range [%d, %d) is not a non-empty subrange of [0, %d)", r0,
+                r1, p->nd);
+  return ZERO_OK;
+}
+
+int check_bound(const zero_plan* p, int32_t r0, int32_t r1) {
+  int rc = check_span(p, r0, r1);
+  if (rc) return rc;
+  if (!p->bound) return fail(ZERO_EUNBOUND, "no state is bound to the plan");
+  if (r0 != p->r0 || r1 != p->r1)
+    return fail(ZERO_EUNBOUND, "rank range [%d, %d) differs from the bound range [%d, %d)", r0,
+                r1, p->r0, p->r1);
+  return ZERO_OK;
+}
+
+int check_device(const zero_plan* p) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != p->device)
+    return fail(ZERO_EINVAL, "current device %d differs from the plan's device %d", dev,
+                p->device);
+  return ZERO_OK;
+}
+
+int check_grads(const zero_plan* p, const void* const* grads) {
+  if (!grads) return fail(ZERO_EINVAL, "grad_ptrs is NULL");
+  for (int k = 0; k < p->nd; ++k) {
+    if (!grads[k]) return fail(ZERO_EINVAL, "grad_ptrs[%d] is NULL", k);
+    if (!aligned16(grads[k])) return fail(ZERO_EALIGN, "grad_ptrs[%d] is not 16-byte aligned", k);
+  }
+  return ZERO_OK;
+}
+
+int check_scalars(float loss_scale, float clip) {
+  if (!std::isfinite(loss_scale) || loss_scale <= 0.0f)
+    return fail(ZERO_EINVAL, "loss_scale must be finite and > 0 (got %g)", (double)loss_scale);
+  if (!std::isfinite(clip)) return fail(ZERO_EINVAL, "clip must be finite (got %g)", (double)clip);
+  return ZERO_OK;
+}
+
+void prof_begin(zero_plan* p, cudaStream_t s, EventPair* ev) {
+  ev->start = nullptr;
+  if (!p->prof || p->pending.size() >= kMaxPendingEvents) return;
+  if (p->free_events.empty()) {
+    EventPair e;
+    if (cudaEventCreate(&e.start) != cudaSuccess) return;
+    if (cudaEventCreate(&e.stop) != cudaSuccess) {
+      cudaEventDestroy(e.start);
+      return;
+    }
+    p->free_events.push_back(e);
+  }
+  *ev = p->free_events.back();
+  p->free_events.pop_back();
+  cudaEventRecord(ev->start, s);
+}
+
+void prof_end(zero_plan* p, cudaStream_t s, EventPair* ev, int kind) {
+  if (!ev->start) return;
+  cudaEventRecord(ev->stop, s);
+  ev->kind = kind;
+  p->pending.push_back(*ev);
+}
+
+int64_t n_valid_of_span(const zero_plan* p) {
+  const int64_t first = (int64_t)p->r0 * p->s;
+  const int64_t n_span = (int64_t)(p->r1 - p->r0) * p->s;
+  return std::max<int64_t>(0, std::min<int64_t>(n_span, p->n - first));
+}
+
+int do_reduce(zero_plan* p, const void* const* grads, bool finalize, float loss_scale,
+              float clip, cudaStream_t s) {
+  // contributions are span-relative: element i of rank k is flat index r0*S + i
+  zero::ReduceLaunch rl{};
+  rl.grads = grads;
+  rl.nd = p->nd;
+  rl.gsum = p->workspace;
+  rl.n_span = (int64_t)(p->r1 - p->r0) * p->s;
+  rl.n_valid = n_valid_of_span(p);
+  rl.scratch = p->scratch;
+  rl.finalize = finalize;
+  rl.loss_scale = loss_scale;
+  rl.clip = clip;
+  rl.hp = p->hp;
+  rl.grid = 0;
+  EventPair ev;
+  prof_begin(p, s, &ev);
+  cudaError_t e = zero::launch_reduce(rl, s);
+  prof_end(p, s, &ev, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  return ZERO_OK;
+}
+
+int do_update(zero_plan* p, cudaStream_t s) {
+  zero::UpdateLaunch ul{};
+  ul.gsum = p->workspace;
+  ul.master = p->master;
+  ul.exp_avg = p->exp_avg;
+  ul.exp_avg_sq = p->exp_avg_sq;
+  ul.param16 = p->param16;
+  ul.n_span = (int64_t)(p->r1 - p->r0) * p->s;
+  ul.n_valid = n_valid_of_span(p);
+  ul.scratch = p->scratch;
+  ul.grid = 0;
+  EventPair ev;
+  prof_begin(p, s, &ev);
+  cudaError_t e = zero::launch_update(ul, s);
+  prof_end(p, s, &ev, 1);
+  if (e != cudaSuccess) return cuda_fail(e, "update launch");
+  return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int zero_plan_create(int64_t n_params, int32_t nd, int32_t stage, int32_t align,
+                     const zero_adam_hparams* hp, zero_plan** out) {
+  g_error.clear();
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (n_params < 1) return fail(ZERO_EINVAL, "n_params must be >= 1");
+  if (nd < 1 || nd > ZERO_MAX_ND) return fail(ZERO_EINVAL, "nd must be in [1, %d]", ZERO_MAX_ND);
+  if (stage < 1 || stage > 3) return fail(ZERO_EINVAL, "stage must be 1, 2 or 3");
+  if (align < 8 || align % 8 != 0) return fail(ZERO_EINVAL, "align must be a positive multiple of 8");
+  if (!hp) return fail(ZERO_EINVAL, "hp is NULL");
+  const float f[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+  for (float x : f)
+    if (!std::isfinite(x)) return fail(ZERO_EINVAL, "hyperparameters must be finite");
+  if (hp->lr < 0 || hp->beta1 < 0 || hp->beta1 >= 1 || hp->beta2 < 0 || hp->beta2 >= 1 ||
+      hp->eps <= 0 || hp->weight_decay < 0)
+    return fail(ZERO_EINVAL, "need lr >= 0, 0 <= beta1, beta2 < 1, eps > 0, weight_decay >= 0");
+  const int64_t unit = (int64_t)nd * align;
+  if (n_params > INT64_MAX - unit) return fail(ZERO_EINVAL, "n_params too large");
+  int64_t np, s;
+  partition(n_params, nd, align, &np, &s);
+  // exact sum of squares: Np * nd^2 * (65504 * 2^24 * (1 + 2^-20))^2 must stay below 2^128
+  const long double bound = (long double)np * nd * nd;
+  if (bound >= 140737488355328.0L)  // 2^47
+    return fail(ZERO_EINVAL, "Np * nd^2 must be below 2^47 (Np = %lld, nd = %d)", (long long)np, nd);
+  zero_plan* p = new (std::nothrow) zero_plan();
+  if (!p) return fail(ZERO_EINVAL, "out of host memory");
+  p->n = n_params;
+  p->np = np;
+  p->s = s;
+  p->nd = nd;
+  p->stage = stage;
+  p->align = align;
+  p->hp = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+  *out = p;
+  return ZERO_OK;
+}
+
+void zero_plan_destroy(zero_plan* p) {
+  if (!p) return;
+  int prev = -1;
+  const bool has_dev = p->device >= 0 && cudaGetDevice(&prev) == cudaSuccess;
+  if (has_dev && prev != p->device) cudaSetDevice(p->device);
+  for (auto& e : p->pending) p->free_events.push_back(e);
+  for (auto& e : p->free_events) {
+    cudaEventDestroy(e.start);
+    cudaEventDestroy(e.stop);
+  }
+  if (p->scratch) cudaFree(p->scratch);
+  if (p->host_sc) cudaFreeHost(p->host_sc);
+  if (has_dev && prev != p->device) cudaSetDevice(prev);
+  delete p;
+}
+
+int zero_plan_layout(const zero_plan* p, int64_t* padded_len, int64_t* shard_len) {
+  g_error.clear();
+  if (!p || !padded_len || !shard_len) return fail(ZERO_EINVAL, "NULL argument");
+  *padded_len = p->np;
+  *shard_len = p->s;
+  return ZERO_OK;
+}
+
+int64_t zero_workspace_bytes(const zero_plan* p, int32_t r0, int32_t r1) {
+  g_error.clear();
+  int rc = check_span(p, r0, r1);
+  if (rc) return rc;
+  return 4 * (int64_t)(r1 - r0) * p->s;
+}
+
+int zero_plan_bind(zero_plan* p, int32_t r0, int32_t r1, float* master, float* exp_avg,
+                   float* exp_avg_sq, void* param16, void* workspace, int64_t initial_step) {
+  g_error.clear();
+  int rc = check_span(p, r0, r1);
+  if (rc) return rc;
+  void* ptrs[5] = {master, exp_avg, exp_avg_sq, param16, workspace};
+  const char* names[5] = {"master", "exp_avg", "exp_avg_sq", "param16", "workspace"};
+  for (int i = 0; i < 5; ++i) {
+    if (!ptrs[i]) return fail(ZERO_EINVAL, "%s is NULL", names[i]);
+    if (!aligned16(ptrs[i])) return fail(ZERO_EALIGN, "%s is not 16-byte aligned", names[i]);
+  }
+  if (initial_step < 0) return fail(ZERO_EINVAL, "initial_step must be >= 0");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->scratch && dev != p->device)
+    return fail(ZERO_EINVAL, "plan was bound on device %d; current device is %d", p->device, dev);
+  if (!p->scratch) {
+    DevScratch* sc = nullptr;
+    e = cudaMalloc(&sc, sizeof(DevScratch));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(scratch)");
+    e = cudaMemset(sc, 0, sizeof(DevScratch));
+    if (e != cudaSuccess) {
+      cudaFree(sc);
+      return cuda_fail(e, "cudaMemset(scratch)");
+    }
+    zero::DevScalars* hs = nullptr;
+    e = cudaMallocHost(&hs, sizeof(zero::DevScalars));
+    if (e != cudaSuccess) {
+      cudaFree(sc);
+      return cuda_fail(e, "cudaMallocHost");
+    }
+    p->scratch = sc;
+    p->host_sc = hs;
+    p->device = dev;
+  }
+  long long t = initial_step;
+  e = cudaMemcpy(&p->scratch->step, &t, sizeof t, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step)");
+  p->bound = true;
+  p->r0 = r0;
+  p->r1 = r1;
+  p->master = master;
+  p->exp_avg = exp_avg;
+  p->exp_avg_sq = exp_avg_sq;
+  p->param16 = param16;
+  p->workspace = static_cast<float*>(workspace);
+  p->stepped = false;
+  return ZERO_OK;
+}
+
+int zero_shard_step(zero_plan* p, int32_t r0, int32_t r1, const void* const* grads,
+                    float loss_scale, float clip, void* stream) {
+  g_error.clear();
+  int rc = check_span(p, r0, r1);
+  if (!rc) rc = check_grads(p, grads);
+  if (!rc) rc = check_scalars(loss_scale, clip);
+  if (!rc) rc = check_bound(p, r0, r1);
+  if (!rc) rc = check_device(p);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = do_reduce(p, grads, true, loss_scale, clip, s);
+  if (rc) return rc;
+  rc = do_update(p, s);
+  if (rc) return rc;
+  p->last_stream = s;
+  p->stepped = true;
+  return ZERO_OK;
+}
+
+int zero_shard_reduce(zero_plan* p, int32_t r0, int32_t r1, const void* const* grads,
+                      void* stream) {
+  g_error.clear();
+  int rc = check_span(p, r0, r1);
+  if (!rc) rc = check_grads(p, grads);
+  if (!rc) rc = check_bound(p, r0, r1);
+  if (!rc) rc = check_device(p);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = do_reduce(p, grads, false, 1.0f, 0.0f, s);
+  if (rc) return rc;
+  p->last_stream = s;
+  return ZERO_OK;
+}
+
+int zero_shard_stats(zero_plan* p, void** dev_words) {
+  g_error.clear();
+  if (!p || !dev_words) return fail(ZERO_EINVAL, "NULL argument");
+  if (!p->scratch) return fail(ZERO_EUNBOUND, "no state is bound to the plan");
+  *dev_words = p->scratch->stats;
+  return ZERO_OK;
+}
+
+int zero_shard_update(zero_plan* p, int32_t r0, int32_t r1, float loss_scale, float clip,
+                      void* stream) {
+  g_error.clear();
+  int rc = check_span(p, r0, r1);
+  if (!rc) rc = check_scalars(loss_scale, clip);
+  if (!rc) rc = check_bound(p, r0, r1);
+  if (!rc) rc = check_device(p);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EventPair ev;
+  prof_begin(p, s, &ev);
+  cudaError_t e = zero::launch_finalize(p->scratch, loss_scale, clip, p->hp, s);
+  prof_end(p, s, &ev, 2);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  rc = do_update(p, s);
+  if (rc) return rc;
+  p->last_stream = s;
+  p->stepped = true;
+  return ZERO_OK;
+}
+
+int zero_step_result(zero_plan* p, zero_step_info* out) {
+  g_error.clear();
+  if (!p || !out) return fail(ZERO_EINVAL, "NULL argument");
+  if (!p->bound || !p->stepped) return fail(ZERO_EUNBOUND, "the plan has not stepped yet");
+  int rc = check_device(p);
+  if (rc) return rc;
+  cudaError_t e = cudaMemcpyAsync(p->host_sc, &p->scratch->sc, sizeof(zero::DevScalars),
+                                  cudaMemcpyDeviceToHost, p->last_stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(p->last_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "step result");
+  const zero::DevScalars& sc = *p->host_sc;
+  std::memset(out, 0, sizeof *out);
+  out->overflow = sc.overflow;
+  out->skipped = sc.skipped;
+  out->status = sc.status;
+  out->step = sc.step;
+  out->global_norm = sc.norm;
+  out->sum_sq = sc.ss;
+  out->clip_coef = sc.clip_coef;
+  out->scale = sc.s;
+  out->bc1 = sc.bc1;
+  out->bc2 = sc.bc2;
+  if (sc.status != 0) return fail(ZERO_EDEVICE, "device status %d", sc.status);
+  return ZERO_OK;
+}
+
+int zero_gather_layers(zero_plan* p, const int64_t* offs, int32_t n_layers,
+                       const void* const* shards, void* const* dst, void* stream) {
+  g_error.clear();
+  if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+  if (!offs || !shards || !dst) return fail(ZERO_EINVAL, "NULL array argument");
+  if (n_layers < 1) return fail(ZERO_EINVAL, "n_layers must be >= 1");
+  if (offs[0] < 0) return fail(ZERO_EINVAL, "layer_offsets[0] must be >= 0");
+  for (int l = 0; l < n_layers; ++l) {
+    if (offs[l + 1] < offs[l]) return fail(ZERO_EINVAL, "layer_offsets must be non-decreasing");
+    if (offs[l + 1] > offs[l]) {
+      if (!dst[l]) return fail(ZERO_EINVAL, "layer_dst[%d] is NULL", l);
+      if (reinterpret_cast<uintptr_t>(dst[l]) & 1u)
+        return fail(ZERO_EALIGN, "layer_dst[%d] is not 2-byte aligned", l);
+    }
+  }
+  if (offs[n_layers] > p->n)
+    return fail(ZERO_EINVAL, "layer_offsets[%d] = %lld exceeds n_params = %lld", n_layers,
+                (long long)offs[n_layers], (long long)p->n);
+  for (int r = 0; r < p->nd; ++r) {
+    if (!shards[r]) return fail(ZERO_EINVAL, "shard_ptrs[%d] is NULL", r);
+    if (reinterpret_cast<uintptr_t>(shards[r]) & 1u)
+      return fail(ZERO_EALIGN, "shard_ptrs[%d] is not 2-byte aligned", r);
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->device >= 0 && dev != p->device)
+    return fail(ZERO_EINVAL, "current device %d differs from the plan's device %d", dev, p->device);
+
+  // Cut each layer at shard boundaries; number the tiles of all segments in order.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  zero::GatherLaunch gl;
+  gl.nseg = 0;
+  gl.tiles = 0;
+  gl.grid = 0;
+  auto flush = [&]() -> int {
+    if (gl.nseg == 0) return ZERO_OK;
+    EventPair ev;
+    prof_begin(p, s, &ev);
+    cudaError_t le = zero::launch_gather(gl, s);
+    prof_end(p, s, &ev, 3);
+    gl.nseg = 0;
+    gl.tiles = 0;
+    if (le != cudaSuccess) return cuda_fail(le, "gather launch");
+    return ZERO_OK;
+  };
+  for (int l = 0; l < n_layers; ++l) {
+    const int64_t a = offs[l], b = offs[l + 1];
+    if (a == b) continue;
+    for (int64_t r = a / p->s; r * p->s < b; ++r) {
+      const int64_t lo = std::max(a, r * p->s), hi = std::min(b, (r + 1) * p->s);
+      if (hi <= lo) continue;
+      if (gl.nseg == zero::kGatherSegs) {
+        int rc = flush();
+        if (rc) return rc;
+      }
+      zero::GatherSeg& sg = gl.seg[gl.nseg++];
+      sg.src = static_cast<const uint16_t*>(shards[r]) + (lo - r * p->s);
+      sg.dst = static_cast<uint16_t*>(dst[l]) + (lo - a);
+      sg.len = hi - lo;
+      sg.tile_begin = gl.tiles;
+      gl.tiles += (sg.len + zero::kGatherTile - 1) / zero::kGatherTile;
+    }
+  }
+  return flush();
+}
+
+int zero_memory_bytes(int64_t n, int32_t nd, int32_t align, int32_t stage, int64_t* out) {
+  g_error.clear();
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  if (n < 1 || nd < 1 || align < 1) return fail(ZERO_EINVAL, "need n >= 1, nd >= 1, align >= 1");
+  int64_t np, s;
+  partition(n, nd, align, &np, &s);
+  switch (stage) {
+    case 0: *out = 16 * n; break;          // replicated: 2 + 2 + 12 bytes per parameter
+    case 1: *out = 4 * n + 12 * s; break;  // optimizer states partitioned
+    case 2: *out = 2 * n + 14 * s; break;  // + gradients
+    case 3: *out = 16 * s; break;          // + parameters
+    default: return fail(ZERO_EINVAL, "stage must be 0, 1, 2 or 3");
+  }
+  return ZERO_OK;
+}
+
+int zero_profile_enable(zero_plan* p, int32_t on) {
+  g_error.clear();
+  if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+  p->prof = on != 0;
+  return ZERO_OK;
+}
+
+int zero_profile_read(zero_plan* p, double* ms, int64_t* launches, int32_t reset) {
+  g_error.clear();
+  if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+  for (auto& ev : p->pending) {
+    cudaError_t e = cudaEventSynchronize(ev.stop);
+    float t = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, ev.start, ev.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "profile events");
+    p->prof_ms[ev.kind] += t;
+    p->prof_launches[ev.kind] += 1;
+    p->free_events.push_back(ev);
+  }
+  p->pending.clear();
+  for (int k = 0; k < ZERO_PROF_KINDS; ++k) {
+    if (ms) ms[k] = p->prof_ms[k];
+    if (launches) launches[k] = p->prof_launches[k];
+    if (reset) {
+      p->prof_ms[k] = 0;
+      p->prof_launches[k] = 0;
+    }
+  }
+  return ZERO_OK;
+}
+
+const char* zero_last_error(void) { return g_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,443 @@
+// Kernels of the ZeRO shard step on sm_103a: the rank-order reduce with the overflow flag
+// and the exact sum of squares, the finalize of the step's scalars, and the fused
+// unscale + clip + AdamW + fp16-cast update.
+//
+// The step is two passes over the span because clipping and the overflow skip need
+// the global norm and flag before any state is written:
+//   reduce:  reads the nd fp16 contributions (2*nd B/param), writes the fp32 sum to the
+//            workspace (4 B/param), and leaves one 128-bit sum of squares and one
+//            non-finite count per CTA; the last CTA to finish combines them.
+//   update:  reads the sum and the fp32 master/m/v (16 B/param), writes master/m/v and
+//            the fp16 parameter (14 B/param).
+// Both kernels are persistent grid-stride loops over groups of 8 elements: every
+// buffer access is one 16-byte vector per thread, coalesced across the warp.
+//
+// Exactness: each summed gradient gsum is an integer multiple of 2^-24 (fp16 values
+// are, and an fp32 sum of them stays one), so k = gsum * 2^24 is an exact integer and
+// the sum of k^2 is carried exactly in 128 bits. The norm therefore does not depend on
+// the grid, the CTA order or the warp shuffle order, and it is rounded once.
+// Every fp32 operation of the update is an explicit round-to-nearest intrinsic (no
+// contraction), so the result is the same bits as a sequential IEEE evaluation.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace zero {
+namespace {
+
+struct U128 {
+  unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ void add128(U128& a, unsigned long long lo, unsigned long long hi) {
+  const unsigned long long l = a.lo + lo;
+  a.hi += hi + (l < lo ? 1ull : 0ull);
+  a.lo = l;
+}
+
+__device__ __forceinline__ bool is_finite(float x) {
+  return (__float_as_uint(x) & 0x7f800000u) != 0x7f800000u;
+}
+
+// (gsum * 2^24)^2 added to a 128-bit accumulator; the caller masks non-finite values.
+__device__ __forceinline__ void add_square(U128& a, float g) {
+  const long long k = __float2ll_rn(__fmul_rn(g, 16777216.0f));
+  const unsigned long long u = (unsigned long long)(k < 0 ? -k : k);
+  add128(a, u * u, __umul64hi(u, u));
+}
+
+// acc0 += fp16 low half of w, acc1 += fp16 high half, each one fp32 add rounded to
+// nearest (sm_100+ mixed-precision add: the fp16 operand is widened exactly).
+__device__ __forceinline__ void add_f16x2(float& acc0, float& acc1, unsigned w) {
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(w));
+}
+
+__device__ __forceinline__ void add_vec(float (&s)[8], const uint4& w) {
+  add_f16x2(s[0], s[1], w.x);
+  add_f16x2(s[2], s[3], w.y);
+  add_f16x2(s[4], s[5], w.z);
+  add_f16x2(s[6], s[7], w.w);
+}
+
+// Correctly rounded conversion of an unsigned 128-bit integer to double.
+__device__ double u128_to_double(U128 a) {
+  if (a.hi == 0) return __ull2double_rn(a.lo);
+  const int lz = __clzll((long long)a.hi);
+  const int shift = 64 - lz;  // 1..64 bits below the top 64
+  unsigned long long top, sticky;
+  if (shift == 64) {
+    top = a.hi;
+    sticky = a.lo;
+  } else {
+    top = (a.hi << lz) | (a.lo >> shift);
+    sticky = a.lo << lz;
+  }
+  // bit 0 of top lies below the 53-bit significand's rounding bit, so or-ing the
+  // dropped bits into it preserves round-to-nearest-even
+  top |= (sticky != 0) ? 1ull : 0ull;
+  return ldexp(__ull2double_rn(top), shift);
+}
+
+// The step's scalars from its statistics (one thread). Double arithmetic, each
+// operation rounded to nearest, then one rounding to fp32.
+__device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float loss_scale,
+                                float clip, const HostHParams& hp) {
+  DevScalars sc;
+  const long long t = st->step;
+  sc.pad = 0;
+  sc.status = 0;
+  sc.ss = __dmul_rn(u128_to_double(ss), 0x1p-48);
+  sc.overflow = bad > 0 ? 1 : 0;
+  sc.skipped = sc.overflow;
+  if (sc.overflow) {
+    sc.norm = __longlong_as_double(0x7ff0000000000000ll);  // +inf
+    sc.clip_coef = 1.0;
+    sc.step = t;
+  } else {
+    sc.norm = __ddiv_rn(__dsqrt_rn(sc.ss), (double)loss_scale);
+    double coef = 1.0;
+    if (clip > 0.0f) {
+      const double c = __ddiv_rn((double)clip, __dadd_rn(sc.norm, 1e-6));
+      if (c < 1.0) coef = c;
+    }
+    sc.clip_coef = coef;
+    sc.step = t + 1;
+  }
+  const double tp = (double)(t + 1);
+  sc.s = __double2float_rn(__ddiv_rn(sc.clip_coef, (double)loss_scale));
+  sc.omb1 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta1));
+  sc.omb2 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta2));
+  sc.bc1 = __double2float_rn(__dadd_rn(1.0, -pow((double)hp.beta1, tp)));
+  sc.bc2 = __double2float_rn(__dadd_rn(1.0, -pow((double)hp.beta2, tp)));
+  sc.decay = __double2float_rn(__dadd_rn(1.0, -__dmul_rn((double)hp.lr, (double)hp.weight_decay)));
+  sc.lr = hp.lr;
+  sc.beta1 = hp.beta1;
+  sc.beta2 = hp.beta2;
+  sc.eps = hp.eps;
+  st->sc = sc;
+  if (!sc.skipped) st->step = t + 1;
+}
+
+// Sum (acc, bad) over the CTA; the result is valid in thread 0.
+__device__ void block_reduce(U128& acc, long long& bad) {
+  __shared__ unsigned long long s_lo[kThreads / 32], s_hi[kThreads / 32];
+  __shared__ long long s_bad[kThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long lo = __shfl_xor_sync(0xffffffffu, acc.lo, o);
+    const unsigned long long hi = __shfl_xor_sync(0xffffffffu, acc.hi, o);
+    bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    add128(acc, lo, hi);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // the shared arrays may still be read by a previous call
+  if (lane == 0) {
+    s_lo[warp] = acc.lo;
+    s_hi[warp] = acc.hi;
+    s_bad[warp] = bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    U128 t{0, 0};
+    long long b = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      add128(t, s_lo[w], s_hi[w]);
+      b += s_bad[w];
+    }
+    acc = t;
+    bad = b;
+  }
+}
+
+template <int CAP>
+struct ReduceArgs {
+  const void* g[CAP];  // rank k's contribution for the span
+  float* gsum;
+  long long n_vec;     // groups of 8 elements in the span
+  long long n_valid;   // real parameters in the span
+  DevScratch* st;
+  float loss_scale, clip;
+  HostHParams hp;
+  int nd;
+  int finalize;
+};
+
+// Sum the contributions of group v in rank order. ND > 0 fixes the rank count at
+// compile time; ND == 0 reads it from the arguments.
+template <int ND, int CAP>
+__device__ __forceinline__ void sum_group(const ReduceArgs<CAP>& a, long long v, float (&s)[8]) {
+  if constexpr (ND > 0 && ND <= 16) {
+    uint4 w[ND];
+#pragma unroll
+    for (int r = 0; r < ND; ++r) w[r] = __ldcs(reinterpret_cast<const uint4*>(a.g[r]) + v);
+#pragma unroll
+    for (int r = 0; r < ND; ++r) add_vec(s, w[r]);
+  } else {
+    const int nd = ND > 0 ? ND : a.nd;
+#pragma unroll 1
+    for (int r0 = 0; r0 < nd; r0 += 8) {
+      uint4 w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (r0 + j < nd) w[j] = __ldcs(reinterpret_cast<const uint4*>(a.g[r0 + j]) + v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (r0 + j < nd) add_vec(s, w[j]);
+    }
+  }
+}
+
+template <int ND, int CAP>
+__global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ ReduceArgs<CAP> a) {
+  U128 acc{0, 0};
+  long long bad = 0;
+  const long long stride = (long long)gridDim.x * kThreads;
+  for (long long v = (long long)blockIdx.x * kThreads + threadIdx.x; v < a.n_vec; v += stride) {
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    sum_group<ND, CAP>(a, v, s);
+    const long long base = v * 8;
+    if (base + 8 <= a.n_valid) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool fin = is_finite(s[j]);
+        bad += fin ? 0 : 1;
+        add_square(acc, fin ? s[j] : 0.0f);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (base + j >= a.n_valid) s[j] = 0.0f;  // padding: not a parameter
+        const bool fin = is_finite(s[j]);
+        bad += fin ? 0 : 1;
+        add_square(acc, fin ? s[j] : 0.0f);
+      }
+    }
+    float4* o = reinterpret_cast<float4*>(a.gsum) + 2 * v;
+    o[0] = make_float4(s[0], s[1], s[2], s[3]);
+    o[1] = make_float4(s[4], s[5], s[6], s[7]);
+  }
+
+  // CTA partial, then the last CTA to arrive combines all partials (no waiting).
+  block_reduce(acc, bad);
+  __shared__ int s_last;
+  DevScratch* st = a.st;
+  if (threadIdx.x == 0) {
+    st->partials[blockIdx.x].lo = acc.lo;
+    st->partials[blockIdx.x].hi = acc.hi;
+    st->partials[blockIdx.x].bad = bad;
+    __threadfence();
+    const unsigned prev = atomicAdd(&st->ticket, 1u);
+    s_last = prev == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  U128 tot{0, 0};
+  long long tb = 0;
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += kThreads) {
+    const DevPartial* p = &st->partials[i];
+    add128(tot, __ldcg(&p->lo), __ldcg(&p->hi));
+    tb += __ldcg(&p->bad);
+  }
+  block_reduce(tot, tb);
+  if (threadIdx.x == 0) {
+    st->stats[0] = tb;
+    st->stats[1] = (long long)(tot.lo & 0xffffffffull);
+    st->stats[2] = (long long)(tot.lo >> 32);
+    st->stats[3] = (long long)(tot.hi & 0xffffffffull);
+    st->stats[4] = (long long)(tot.hi >> 32);
+    st->stats[5] = st->stats[6] = st->stats[7] = 0;
+    if (a.finalize) compute_scalars(st, tb, tot, a.loss_scale, a.clip, a.hp);
+    st->ticket = 0;
+  }
+}
+
+// Scalars from the exchange buffer, after the caller's all-reduce (one thread).
+__global__ void k_finalize(DevScratch* st, float loss_scale, float clip, HostHParams hp) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const long long bad = st->stats[0];
+  U128 ss{0, 0};
+  for (int i = 0; i < 4; ++i) {
+    const unsigned long long l = (unsigned long long)st->stats[1 + i];
+    switch (i) {
+      case 0: add128(ss, l, 0ull); break;
+      case 1: add128(ss, l << 32, l >> 32); break;
+      case 2: add128(ss, 0ull, l); break;
+      default: add128(ss, 0ull, l << 32); break;
+    }
+  }
+  compute_scalars(st, bad, ss, loss_scale, clip, hp);
+}
+
+struct UpdateArgs {
+  const float* gsum;
+  float *master, *m, *v;
+  uint16_t* p16;
+  long long n_valid;
+  DevScratch* st;
+};
+
+struct Sc {
+  float s, b1, b2, omb1, omb2, bc1, bc2, eps, decay, lr;
+};
+
+__device__ __forceinline__ float adam_elem(float gs, float p0, float& m, float& v, const Sc& c) {
+  const float g = __fmul_rn(gs, c.s);
+  m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
+  v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
+  const float mh = __fdiv_rn(m, c.bc1);
+  const float vh = __fdiv_rn(v, c.bc2);
+  const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), c.eps));
+  const float p = __fmul_rn(p0, c.decay);
+  return __fsub_rn(p, __fmul_rn(c.lr, u));
+}
+
+__device__ __forceinline__ unsigned pack_h2(float a, float b) {
+  const __half2 h = __halves2half2(__float2half_rn(a), __float2half_rn(b));
+  return *reinterpret_cast<const unsigned*>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ UpdateArgs a) {
+  const DevScalars* scp = &a.st->sc;
+  if (scp->skipped) return;  // overflow: the state keeps its bits
+  Sc c;
+  c.s = scp->s;
+  c.b1 = scp->beta1;
+  c.b2 = scp->beta2;
+  c.omb1 = scp->omb1;
+  c.omb2 = scp->omb2;
+  c.bc1 = scp->bc1;
+  c.bc2 = scp->bc2;
+  c.eps = scp->eps;
+  c.decay = scp->decay;
+  c.lr = scp->lr;
+
+  const long long n_full = a.n_valid >> 3;  // groups made only of real parameters
+  const long long stride = (long long)gridDim.x * kThreads;
+  const float4* g4 = reinterpret_cast<const float4*>(a.gsum);
+  float4* p4 = reinterpret_cast<float4*>(a.master);
+  float4* m4 = reinterpret_cast<float4*>(a.m);
+  float4* v4 = reinterpret_cast<float4*>(a.v);
+  uint4* h4 = reinterpret_cast<uint4*>(a.p16);
+  for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < n_full; i += stride) {
+    const float4 ga = __ldcs(g4 + 2 * i), gb = __ldcs(g4 + 2 * i + 1);
+    const float4 pa = __ldcs(p4 + 2 * i), pb = __ldcs(p4 + 2 * i + 1);
+    float4 ma = __ldcs(m4 + 2 * i), mb = __ldcs(m4 + 2 * i + 1);
+    float4 va = __ldcs(v4 + 2 * i), vb = __ldcs(v4 + 2 * i + 1);
+    float4 qa, qb;
+    qa.x = adam_elem(ga.x, pa.x, ma.x, va.x, c);
+    qa.y = adam_elem(ga.y, pa.y, ma.y, va.y, c);
+    qa.z = adam_elem(ga.z, pa.z, ma.z, va.z, c);
+    qa.w = adam_elem(ga.w, pa.w, ma.w, va.w, c);
+    qb.x = adam_elem(gb.x, pb.x, mb.x, vb.x, c);
+    qb.y = adam_elem(gb.y, pb.y, mb.y, vb.y, c);
+    qb.z = adam_elem(gb.z, pb.z, mb.z, vb.z, c);
+    qb.w = adam_elem(gb.w, pb.w, mb.w, vb.w, c);
+    __stcs(p4 + 2 * i, qa);
+    __stcs(p4 + 2 * i + 1, qb);
+    __stcs(m4 + 2 * i, ma);
+    __stcs(m4 + 2 * i + 1, mb);
+    __stcs(v4 + 2 * i, va);
+    __stcs(v4 + 2 * i + 1, vb);
+    __stcs(h4 + i, make_uint4(pack_h2(qa.x, qa.y), pack_h2(qa.z, qa.w), pack_h2(qb.x, qb.y),
+                              pack_h2(qb.z, qb.w)));
+  }
+  // The group that holds the end of the real parameters: element-wise, real ones only.
+  const long long rem = a.n_valid & 7;
+  if (rem != 0 && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+    const long long b = n_full * 8;
+    for (long long j = b; j < b + rem; ++j) {
+      float m = a.m[j], v = a.v[j];
+      const float p = adam_elem(a.gsum[j], a.master[j], m, v, c);
+      a.master[j] = p;
+      a.m[j] = m;
+      a.v[j] = v;
+      const __half h = __float2half_rn(p);
+      a.p16[j] = *reinterpret_cast<const uint16_t*>(&h);
+    }
+  }
+}
+
+template <typename K>
+int occupancy_grid(K kernel, long long work_items) {
+  static thread_local int cached_dev = -1;
+  static thread_local int sms = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != cached_dev) {
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cached_dev = dev;
+  }
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+  if (per_sm < 1) per_sm = 1;
+  long long g = (long long)sms * per_sm;
+  const long long need = (work_items + kThreads - 1) / kThreads;
+  if (g > need) g = need;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+template <int ND, int CAP>
+cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s) {
+  ReduceArgs<CAP> a;
+  for (int r = 0; r < CAP; ++r) a.g[r] = r < p.nd ? p.grads[r] : nullptr;
+  a.gsum = p.gsum;
+  a.n_vec = p.n_span / 8;
+  a.n_valid = p.n_valid;
+  a.st = p.scratch;
+  a.loss_scale = p.loss_scale;
+  a.clip = p.clip;
+  a.hp = p.hp;
+  a.nd = p.nd;
+  a.finalize = p.finalize ? 1 : 0;
+  int grid = occupancy_grid(k_reduce<ND, CAP>, a.n_vec);
+  if (grid > kMaxPartialBlocks) grid = kMaxPartialBlocks;
+  if (p.grid > 0 && p.grid < grid) grid = p.grid;
+  k_reduce<ND, CAP><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s) {
+  switch (p.nd) {
+    case 1: return go_reduce<1, 16>(p, s);
+    case 2: return go_reduce<2, 16>(p, s);
+    case 4: return go_reduce<4, 16>(p, s);
+    case 8: return go_reduce<8, 16>(p, s);
+    case 16: return go_reduce<16, 16>(p, s);
+    case 32: return go_reduce<32, 64>(p, s);
+    case 64: return go_reduce<64, 64>(p, s);
+    default:
+      if (p.nd <= 64) return go_reduce<0, 64>(p, s);
+      return go_reduce<0, ZERO_MAX_ND>(p, s);
+  }
+}
+
+cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,
+                            const HostHParams& hp, cudaStream_t s) {
+  k_finalize<<<1, 32, 0, s>>>(scratch, loss_scale, clip, hp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s) {
+  UpdateArgs a;
+  a.gsum = p.gsum;
+  a.master = p.master;
+  a.m = p.exp_avg;
+  a.v = p.exp_avg_sq;
+  a.p16 = static_cast<uint16_t*>(p.param16);
+  a.n_valid = p.n_valid;
+  a.st = p.scratch;
+  int grid = occupancy_grid(k_update, (p.n_valid + 7) / 8);
+  if (p.grid > 0 && p.grid < grid) grid = p.grid;
+  k_update<<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace zero

@@ -1,0 +1,205 @@
+"""GPU parity of the shard step through the C ABI against the oracle, element by element.
+
+Sizes here are ones the oracle finishes in seconds: they span many CTAs and grid-stride
+rounds, ragged shard tails (padding) and every rank count the kernels specialise.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sharded_emulated_reduce_gb300 as z
+from synth import workloads as wl
+
+from parity import Runner, assert_info_matches, device_words, h16, f32, hyper
+
+pytestmark = pytest.mark.gpu
+
+TINY = wl.WORKLOADS["zero2_tiny_1m_nd4"]
+
+
+def small(**kw) -> wl.Workload:
+    base = dict(name="small", cfg=100, n=4099, nd=4, align=8, stage=2, r0=0, r1=4,
+                loss_scale=1024.0, grad_sigma=1e-3, clip=1.0, steps=3, m_sigma=1e-3,
+                v_sigma=1e-6)
+    base.update(kw)
+    return wl.Workload(**base)
+
+
+def test_tiny_zero2_workload_all_steps_bit_exact():
+    r = Runner(TINY).run()
+    assert len(r.results) == TINY.steps and all(x["skipped"] == 0 for x in r.results)
+    assert r.exact
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 1023, 4099, 70001])
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 8, 16, 17, 32, 64, 100])
+def test_odd_shapes_and_rank_counts(n, nd):
+    if n * nd > 2_000_000:
+        n = 2_000_000 // nd
+    r = Runner(small(n=n, nd=nd, r1=nd, cfg=101 + nd)).run()
+    assert r.exact
+
+
+@pytest.mark.parametrize("align", [8, 16, 128])
+@pytest.mark.parametrize("r0,r1", [(0, 1), (1, 3), (2, 3), (0, 3)])
+def test_rank_subranges_and_alignment(align, r0, r1):
+    w = small(n=10_000, nd=3, align=align, r0=r0, r1=r1, cfg=130 + align + r0 * 7 + r1)
+    assert Runner(w).run().exact
+
+
+def test_span_entirely_in_padding():
+    # N = 5, Nd = 4, align = 8: shards 1..3 hold only padding
+    w = small(n=5, nd=4, r0=2, r1=4, cfg=140)
+    r = Runner(w).run()
+    assert all(x["global_norm"] == 0.0 and x["step"] == i + 1 for i, x in enumerate(r.results))
+
+
+@pytest.mark.parametrize("where", ["first", "middle", "last", "padding"])
+@pytest.mark.parametrize("rank", ["first", "last"])
+@pytest.mark.parametrize("value", [wl.POS_INF, wl.NEG_INF, wl.QNAN])
+def test_overflow_injection(where, rank, value):
+    n, nd = 4990, 5  # padded to 5000: ten padding elements
+    idx = {"first": 0, "middle": n // 2, "last": n - 1, "padding": n + 3}[where]
+    rk = 0 if rank == "first" else nd - 1
+    w = small(n=n, nd=nd, r1=nd, steps=3, cfg=150, inject=((1, rk, value, idx),))
+    r = Runner(w).run()
+    skipped = [x["skipped"] for x in r.results]
+    assert skipped == ([0, 0, 0] if where == "padding" else [0, 1, 0])
+    assert [x["step"] for x in r.results] == ([1, 2, 3] if where == "padding" else [1, 1, 2])
+    assert r.exact
+
+
+def test_opposite_infinities_in_two_ranks_make_nan_and_skip():
+    w = small(n=3000, nd=4, steps=2, cfg=160,
+              inject=((0, 0, wl.POS_INF, 1234), (0, 3, wl.NEG_INF, 1234)))
+    r = Runner(w).run()
+    assert [x["skipped"] for x in r.results] == [1, 0]
+
+
+def test_clip_off_and_on_and_mean_loss_scale():
+    for clip, ls in [(0.0, 1024.0), (1e-3, 1024.0), (1e6, 4096.0), (1.0, 4.0 * 1024.0)]:
+        assert Runner(small(n=20_000, clip=clip, loss_scale=ls, cfg=170)).run().exact
+
+
+def test_two_runs_are_bit_identical():
+    outs = []
+    for _ in range(2):
+        r = Runner(small(n=300_000, nd=8, r1=8, cfg=180, steps=2)).run()
+        outs.append([f32(t).copy() if t.dtype == torch.float32 else h16(t).copy()
+                     for t in r.state[:4]])
+        r.plan.close()
+    for a, b in zip(*outs):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_split_reduce_update_equals_fused_step():
+    w = small(n=200_000, nd=8, r1=8, cfg=190, steps=3)
+    first, n_span, n_valid = w.span()
+    states = []
+    infos = []
+    for split in (False, True):
+        master, m, v, p16, ws = wl.make_state(w)
+        plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+        z.zero_plan_bind(plan, w.r0, w.r1, master, m, v, p16, ws, 0)
+        grads = [torch.empty(n_span, dtype=torch.float16, device="cuda") for _ in range(w.nd)]
+        inf = []
+        for step in range(w.steps):
+            wl.fill_grads(w, step, grads)
+            if split:
+                z.zero_shard_reduce(plan, w.r0, w.r1, grads)
+                words = z.zero_shard_stats(plan)
+                assert words % 8 == 0
+                z.zero_shard_update(plan, w.r0, w.r1, w.loss_scale, w.clip)
+            else:
+                z.zero_shard_step(plan, w.r0, w.r1, grads, w.loss_scale, w.clip)
+            inf.append(z.zero_step_result(plan).as_dict())
+        states.append([f32(master), f32(m), f32(v), h16(p16)])
+        infos.append(inf)
+        plan.close()
+    assert infos[0] == infos[1]
+    for a, b in zip(*states):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_exchange_buffer_holds_the_oracle_statistics():
+    w = small(n=50_000, nd=4, cfg=200, steps=1)
+    first, n_span, n_valid = w.span()
+    master, m, v, p16, ws = wl.make_state(w)
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, 0, 4, master, m, v, p16, ws, 0)
+    grads = wl.make_grads(w, 0)
+    z.zero_shard_reduce(plan, 0, 4, grads)
+    torch.cuda.synchronize()
+    got = device_words(z.zero_shard_stats(plan), z.ZERO_STATS_WORDS).tolist()
+    bad, ss = oracle.stats(oracle.reduce([h16(g) for g in grads], n_valid))
+    assert got[0] == bad
+    assert sum(got[1 + i] << (32 * i) for i in range(4)) == ss
+    assert got[5:] == [0, 0, 0]
+
+
+def test_profile_counts_every_launch():
+    w = small(n=100_000, nd=4, cfg=210, steps=1)
+    first, n_span, n_valid = w.span()
+    master, m, v, p16, ws = wl.make_state(w)
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, 0, 4, master, m, v, p16, ws, 0)
+    z.zero_profile_enable(plan, True)
+    grads = wl.make_grads(w, 0)
+    for _ in range(5):
+        z.zero_shard_step(plan, 0, 4, grads, w.loss_scale, w.clip)
+    z.zero_shard_reduce(plan, 0, 4, grads)
+    z.zero_shard_update(plan, 0, 4, w.loss_scale, w.clip)
+    ms, n = z.zero_profile_read(plan, reset=True)
+    assert n[:3] == [6, 6, 1] and all(x > 0 for x in ms[:3])
+    ms, n = z.zero_profile_read(plan)
+    assert n == [0, 0, 0, 0]
+
+
+def test_step_counter_continues_from_initial_step():
+    w = small(n=4096, cfg=220, steps=1)
+    first, n_span, n_valid = w.span()
+    master, m, v, p16, ws = wl.make_state(w)
+    om, omm, ov, op = f32(master).copy(), f32(m).copy(), f32(v).copy(), h16(p16).copy()
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, 0, 4, master, m, v, p16, ws, 41)
+    grads = wl.make_grads(w, 0)
+    z.zero_shard_step(plan, 0, 4, grads, w.loss_scale, w.clip)
+    info = z.zero_step_result(plan)
+    sc = oracle.step([h16(g) for g in grads], om, omm, ov, op, w.loss_scale, w.clip, hyper(w),
+                     41, n_valid=n_valid)
+    assert info.step == 42
+    assert_info_matches(info, sc)
+    assert np.array_equal(f32(master).view(np.uint32), om.view(np.uint32))
+
+
+def test_wrong_device_state_and_stream_usage():
+    w = small(n=4096, cfg=230, steps=1)
+    master, m, v, p16, ws = wl.make_state(w)
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, 0, 4, master, m, v, p16, ws, 0)
+    grads = wl.make_grads(w, 0)
+    with pytest.raises(z.ZeroError) as ei:
+        z.zero_shard_step(plan, 0, 3, grads, 1.0, 0.0)   # not the bound span
+    assert ei.value.code == z.ZERO_EUNBOUND
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        z.zero_shard_step(plan, 0, 4, grads, w.loss_scale, w.clip)
+    assert z.zero_step_result(plan).step == 1
+
+
+def test_device_generator_matches_cpu_generator():
+    import synth
+    key = synth.stream_key(0, synth.GRAD, 7, 3, 2)
+    for dtype, sigma in [(torch.float16, 65.536), (torch.float32, 0.02), (torch.float32, -1e-6)]:
+        t = torch.empty(100_003, dtype=dtype, device="cuda")
+        synth.fill(t, key, sigma, start=12345, n_valid=12345 + 90_000)
+        if dtype == torch.float16:
+            ref = synth.values_f16(key, sigma, 12345, 100_003, n_valid=12345 + 90_000)
+            assert np.array_equal(h16(t), ref)
+        else:
+            ref = synth.values_f32(key, abs(sigma), 12345, 100_003, n_valid=12345 + 90_000,
+                                   absolute=sigma < 0)
+            assert np.array_equal(f32(t).view(np.uint32), ref.view(np.uint32))
