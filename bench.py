@@ -236,33 +236,21 @@ def run_ours(args, w0):
         dist.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
-    if w0.nd % world:
-        raise SystemExit(f"--gpus {world} must divide Nd = {w0.nd}")
-    per = w0.nd // world
-    w = dataclasses.replace(w0, r0=rank * per, r1=(rank + 1) * per)
+    r0, r1 = z.rank_ranges(w0.nd, world)[rank]
+    w = dataclasses.replace(w0, r0=r0, r1=r1)
     first, n_span, n_valid = w.span()
     dev = torch.device("cuda", torch.cuda.current_device())
 
     master, m, v, p16, ws = wl.make_state(w, dev)
-    gsets = [wl.make_grads(w, s, dev) for s in range(2)]
+    gsets = [wl.make_grads(w, s, dev) for s in range(1 if args.one_set else 2)]
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
     z.zero_plan_bind(plan, w.r0, w.r1, master, m, v, p16, ws, 0)
     stream = torch.cuda.current_stream()
-    stats_t = None
-    if dist is not None:
-        stats_t = torch.zeros(z.ZERO_STATS_WORDS, dtype=torch.int64, device=dev)
-        stats_addr = z.zero_shard_stats(plan)
-
     def one_step(grads):
         if dist is None:
             z.zero_shard_step(plan, w.r0, w.r1, grads, w.loss_scale, w.clip, stream)
         else:
-            z.zero_shard_reduce(plan, w.r0, w.r1, grads, stream)
-            # exchange: sum the statistics words of all ranks (exact integers)
-            copy_words(stats_addr, stats_t, to_tensor=True)
-            dist.all_reduce(stats_t)
-            copy_words(stats_addr, stats_t, to_tensor=False)
-            z.zero_shard_update(plan, w.r0, w.r1, w.loss_scale, w.clip, stream)
+            z.zero_dist_step(plan, w.r0, w.r1, grads, w.loss_scale, w.clip, stream=stream)
 
     def barrier():
         if dist is not None:
@@ -270,7 +258,7 @@ def run_ours(args, w0):
         torch.cuda.synchronize()
 
     for i in range(args.warmup):
-        one_step(gsets[i % 2])
+        one_step(gsets[i % len(gsets)])
     barrier()
 
     clocks = ClockSampler(local)
@@ -283,7 +271,7 @@ def run_ours(args, w0):
     clocks.mark("start")
     e0.record(stream)
     for i in range(args.steps):
-        one_step(gsets[i % 2])
+        one_step(gsets[i % len(gsets)])
     e1.record(stream)
     barrier()
     clocks.mark("end")
@@ -302,26 +290,30 @@ def run_ours(args, w0):
 
     # e2e through the public API with host buffers: per step the H2D copy of the step's
     # gradients from pinned host memory, the step, and the D2H read of its result
-    host = [[g.cpu().pin_memory() for g in gs] for gs in gsets]
-    dev_g = [torch.empty_like(g) for g in gsets[0]]
-    e2e_steps = max(3, min(args.steps, 100))
-    for i in range(2):
-        for d, h in zip(dev_g, host[i % 2]):
-            d.copy_(h, non_blocking=True)
-        one_step(dev_g)
-        z.zero_step_result(plan)
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        for d, h in zip(dev_g, host[i % 2]):
-            d.copy_(h, non_blocking=True)
-        one_step(dev_g)
-        z.zero_step_result(plan)
-    barrier()
-    e2e_s = torch.tensor([(time.perf_counter() - t0) / e2e_steps], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(e2e_s, op=dist.ReduceOp.MAX)
-    e2e_value = total_params / e2e_s.item()
+    e2e_steps = 0
+    e2e_value = None
+    if not args.no_e2e:
+        host = [[g.cpu().pin_memory() for g in gs] for gs in gsets]
+        dev_g = [torch.empty_like(g) for g in gsets[0]]
+        e2e_steps = max(3, min(args.steps, 100))
+        for i in range(2):
+            for d, h in zip(dev_g, host[i % len(host)]):
+                d.copy_(h, non_blocking=True)
+            one_step(dev_g)
+            z.zero_step_result(plan)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            for d, h in zip(dev_g, host[i % len(host)]):
+                d.copy_(h, non_blocking=True)
+            one_step(dev_g)
+            z.zero_step_result(plan)
+        barrier()
+        e2e_s = torch.tensor([(time.perf_counter() - t0) / e2e_steps], dtype=torch.float64,
+                             device=dev)
+        if dist is not None:
+            dist.all_reduce(e2e_s, op=dist.ReduceOp.MAX)
+        e2e_value = total_params / e2e_s.item()
     h2d = sum(g.numel() * g.element_size() for g in gsets[0]) * world
 
     peak, peak_kind = load_peaks()
@@ -372,21 +364,6 @@ def run_ours(args, w0):
     return 0
 
 
-def copy_words(addr, tensor, to_tensor: bool):
-    """Device-to-device copy between the plan's statistics words and a torch tensor."""
-    import ctypes
-
-    import torch
-    cudart = ctypes.CDLL("libcudart.so.13")
-    n = tensor.numel() * 8
-    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    dst, src = (tensor.data_ptr(), addr) if to_tensor else (addr, tensor.data_ptr())
-    rc = cudart.cudaMemcpyAsync(ctypes.c_void_p(dst), ctypes.c_void_p(src), ctypes.c_size_t(n),
-                                3, stream)  # cudaMemcpyDeviceToDevice
-    if rc != 0:
-        raise RuntimeError(f"cudaMemcpyAsync failed: {rc}")
-
-
 def load_traffic(kernel: str, w):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the same
     kernel source and workload; None otherwise."""
@@ -416,6 +393,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU oracle baseline budget (0 skips it)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--one-set", action="store_true",
+                    help="one gradient set instead of two (less device memory)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -250,3 +250,57 @@ def zero_profile_read(plan: Plan, reset: bool = False) -> tuple[list[float], lis
     n = (_I64 * ZERO_PROF_KINDS)()
     _check(_lib.zero_profile_read(plan, ms, n, 1 if reset else 0))
     return list(ms), list(n)
+
+
+# ------------------------------------------------------------------------------------
+# Spans split across processes (one process per GPU)
+
+def rank_ranges(nd: int, world: int) -> list[tuple[int, int]]:
+    """The logical-rank span [r0, r1) of each of ``world`` processes: contiguous, equal
+    sized, in process order. ``world`` must divide ``nd``."""
+    if world < 1 or nd % world:
+        raise ValueError(f"world size {world} must divide Nd = {nd}")
+    per = nd // world
+    return [(g * per, (g + 1) * per) for g in range(world)]
+
+
+def stats_words(nonfinite: int, sum_sq: int) -> list[int]:
+    """Host view of the exchange-buffer format (zero_shard_stats): word 0 the non-finite
+    count, words 1..4 the 32-bit limbs of the exact sum of squares of (gsum * 2^24),
+    least significant first, words 5..7 zero."""
+    return [nonfinite] + [(sum_sq >> (32 * i)) & 0xFFFFFFFF for i in range(4)] + [0, 0, 0]
+
+
+def stats_decode(words: Sequence[int]) -> tuple[int, int]:
+    """(non-finite count, exact sum of squares) of a (possibly summed) exchange buffer."""
+    return int(words[0]), sum(int(words[1 + i]) << (32 * i) for i in range(4))
+
+
+class _DeviceWords:
+    """__cuda_array_interface__ over the plan's device statistics words."""
+
+    def __init__(self, addr: int):
+        self.__cuda_array_interface__ = {"shape": (ZERO_STATS_WORDS,), "typestr": "<i8",
+                                         "data": (addr, False), "version": 3, "strides": None}
+
+
+def stats_tensor(plan: Plan):
+    """A torch int64 tensor aliasing the plan's exchange buffer on its device."""
+    import torch
+    return torch.as_tensor(_DeviceWords(zero_shard_stats(plan)), device="cuda")
+
+
+def zero_dist_step(plan: Plan, r0: int, r1: int, grads: Sequence, loss_scale: float,
+                   clip: float, group=None, stream=None) -> None:
+    """One shard step of a span split across the processes of a torch.distributed group:
+    zero_shard_reduce, an integer sum all-reduce of the statistics words (the exchange
+    step; exact, so the result does not depend on the reduction order), then
+    zero_shard_update. Every process calls it with its own span."""
+    import torch
+    import torch.distributed as dist
+    s = torch.cuda.current_stream() if stream is None else stream
+    zero_shard_reduce(plan, r0, r1, grads, s)
+    words = stats_tensor(plan)
+    with torch.cuda.stream(s):
+        dist.all_reduce(words, op=dist.ReduceOp.SUM, group=group)
+    zero_shard_update(plan, r0, r1, loss_scale, clip, s)

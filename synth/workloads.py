@@ -93,6 +93,11 @@ WORKLOADS = {
         # 7B ZeRO-2: this device is rank 0 and owns S = 875M parameters
         Workload("zero2_7b_rank0_nd8", cfg=3, n=7_000_000_000, nd=8, align=8, stage=2, r0=0,
                  r1=1, loss_scale=1024.0, grad_sigma=1e-3, clip=1.0, steps=5),
+        # the GPT-2-small recipe on a 32M-parameter buffer (1 GB on the device): a case
+        # small enough for detailed profiler captures, still far larger than L2
+        Workload("flat_32m_nd8", cfg=5, n=33_554_432, nd=8, align=128, stage=2, r0=0, r1=8,
+                 loss_scale=65536.0, grad_sigma=1e-3, clip=1.0, steps=3,
+                 m_sigma=1e-3, v_sigma=1e-6),
         # 13B, 40 layers of 325M, ZeRO-3: rank 0's step over S ~ 203M, then the gather of
         # all 64 fp16 shards into the 40 layer buffers
         Workload("zero3_13b_rank0_nd64", cfg=4, n=13_000_000_000, nd=64, align=8, stage=3, r0=0,

@@ -203,3 +203,40 @@ def test_device_generator_matches_cpu_generator():
             ref = synth.values_f32(key, abs(sigma), 12345, 100_003, n_valid=12345 + 90_000,
                                    absolute=sigma < 0)
             assert np.array_equal(f32(t).view(np.uint32), ref.view(np.uint32))
+
+
+def test_dist_step_in_one_process_group_equals_step():
+    import os
+    import socket
+    import torch.distributed as dist
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        w = small(n=123_457, nd=8, r1=8, cfg=240, steps=3,
+                  inject=((1, 2, wl.POS_INF, 999),))
+        first, n_span, n_valid = w.span()
+        states, infos = [], []
+        for use_dist in (False, True):
+            master, m, v, p16, ws = wl.make_state(w)
+            plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+            z.zero_plan_bind(plan, 0, 8, master, m, v, p16, ws, 0)
+            grads = [torch.empty(n_span, dtype=torch.float16, device="cuda") for _ in range(8)]
+            inf = []
+            for step in range(w.steps):
+                wl.fill_grads(w, step, grads)
+                if use_dist:
+                    z.zero_dist_step(plan, 0, 8, grads, w.loss_scale, w.clip)
+                else:
+                    z.zero_shard_step(plan, 0, 8, grads, w.loss_scale, w.clip)
+                inf.append(z.zero_step_result(plan).as_dict())
+            states.append([f32(master), f32(m), f32(v), h16(p16)])
+            infos.append(inf)
+            plan.close()
+        assert infos[0] == infos[1] and [x["skipped"] for x in infos[0]] == [0, 1, 0]
+        for a, b in zip(*states):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    finally:
+        dist.destroy_process_group()
