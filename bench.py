@@ -236,7 +236,10 @@ def run_ours(args, w0):
         dist.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
-    r0, r1 = z.rank_ranges(w0.nd, world)[rank]
+    # split the workload's own span of logical ranks across the processes
+    if (w0.r1 - w0.r0) % world:
+        raise SystemExit(f"--gpus {world} must divide the span's {w0.r1 - w0.r0} logical ranks")
+    r0, r1 = [(w0.r0 + a, w0.r0 + b) for a, b in z.rank_ranges(w0.r1 - w0.r0, world)][rank]
     w = dataclasses.replace(w0, r0=r0, r1=r1)
     first, n_span, n_valid = w.span()
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -383,6 +386,71 @@ def load_traffic(kernel: str, w):
     return ent.get("dram_bytes_per_launch")
 
 
+def run_gather(args, w):
+    """Time the ZeRO-3 gather of all Nd fp16 shards into the workload's layer buffers."""
+    import torch
+
+    import sharded_emulated_reduce_gb300 as z
+    from synth import workloads as wl
+
+    if env_int("WORLD_SIZE", 1) > 1 and env_int("RANK", 0) != 0:
+        return 0
+    torch.cuda.set_device(0)
+    if not w.layers:
+        raise SystemExit(f"workload {w.name} has no layer table")
+    _, s = w.layout()
+    shard0 = torch.empty(s, dtype=torch.float16, device="cuda")
+    shards = wl.make_shards(w, shard0)
+    wl.fill(shard0, wl.key(w, wl.SHARD16, 0, 0), w.shard_sigma, start=0, n_valid=w.n)
+    offs = list(w.layers)
+    dst = [torch.empty(offs[l + 1] - offs[l], dtype=torch.float16, device="cuda")
+           for l in range(len(offs) - 1)]
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        z.zero_gather_layers(plan, offs, shards, dst, stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    z.zero_profile_enable(plan, True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark("start")
+    e0.record(stream)
+    for _ in range(args.steps):
+        z.zero_gather_layers(plan, offs, shards, dst, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("end")
+    ms = e0.elapsed_time(e1) / args.steps
+    kms, kl = z.zero_profile_read(plan, reset=True)
+    clk = clocks.stop()
+    n_moved = offs[-1] - offs[0]
+    peak, peak_kind = load_peaks()
+    avg = kms[z.PROF_GATHER] / kl[z.PROF_GATHER]  # per launch
+    launches_per_call = kl[z.PROF_GATHER] // args.steps
+    alg = 4 * n_moved / launches_per_call
+    achieved = alg / (avg / 1e3) / 1e9
+    line = {
+        "metric": "ZeRO-3 gather params/s (fp16 shards to layer buffers); achieved HBM GB/s "
+                  "as % of GB300 peak",
+        "value": n_moved / (ms / 1e3), "unit": "params/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "f16 (copy)", "data": "synthetic",
+        "config": {"workload": w.name, "op": "gather", "n_params": w.n, "nd": w.nd,
+                   "layers": len(offs) - 1, "shard_len": s,
+                   "l2": f"inputs larger than L2 ({2 * w.n / 1e9:.1f} GB of shards); no flush"},
+        "e2e": None, "gpu_launches": int(kl[z.PROF_GATHER]),
+        "roofline": {"bound": "hbm", "kernel": "gather", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": None, "alg_bytes_per_launch": alg, "avg_launch_ms": avg},
+        "cpu_baseline": None, "clocks": clk,
+    }
+    print(json.dumps(line))
+    plan.close()
+    return 0
+
+
 def main(argv=None):
     from synth import workloads as wl
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -391,6 +459,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="gpt2_small_flat_nd8", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="step", choices=["step", "gather"],
+                    help="the shard step (default) or the ZeRO-3 gather")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU oracle baseline budget (0 skips it)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
@@ -402,6 +472,8 @@ def main(argv=None):
     w = wl.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.op == "gather":
+        return run_gather(args, w)
     return run_ours(args, w)
 
 

@@ -85,6 +85,9 @@ def lib():
             L.oracle_step.argtypes = [_I32, _P, _I64, _I64, _P, _P, _P, _P, _P,
                                       ctypes.c_float, ctypes.c_float, ctypes.POINTER(HParams),
                                       _I64, ctypes.POINTER(Scalars)]
+            L.oracle_scaler_update.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                               ctypes.POINTER(_I32), _I32, ctypes.c_float,
+                                               ctypes.c_float, _I32]
             L.oracle_gather.argtypes = [_I32, _I64, _P, _I32, _P, _P]
             L.oracle_gather_source.argtypes = [_I64, _I64, ctypes.POINTER(_I32),
                                                ctypes.POINTER(_I64)]
@@ -211,3 +214,13 @@ def gather_source(shard_len: int, i: int) -> tuple[int, int]:
     r, off = _I32(), _I64()
     lib().oracle_gather_source(shard_len, i, ctypes.byref(r), ctypes.byref(off))
     return r.value, off.value
+
+
+def scaler_update(scale: float, good_steps: int, overflow: bool, growth: float = 2.0,
+                  backoff: float = 0.5, interval: int = 2000) -> tuple[float, int]:
+    """(new fp32 scale, new good-step count) after one step."""
+    sc = ctypes.c_float(scale)
+    g = _I32(good_steps)
+    lib().oracle_scaler_update(ctypes.byref(sc), ctypes.byref(g), 1 if overflow else 0, growth,
+                               backoff, interval)
+    return sc.value, g.value

@@ -267,6 +267,27 @@ void oracle_step(int32_t nd, const uint16_t* const* contrib, int64_t n, int64_t 
 }
 
 /* ---------------------------------------------------------------------------------
+ * Dynamic loss scale. The pages say only "mixed precision"; the scaler is the usual
+ * companion of a skipped overflow step: back off on overflow, grow after a run of good
+ * steps.
+ */
+void oracle_scaler_update(float* scale, int32_t* good_steps, int32_t overflow, float growth,
+                          float backoff, int32_t interval) {
+  if (overflow) {
+    *scale = *scale * backoff;
+    *good_steps = 0;
+    return;
+  }
+  int32_t good = *good_steps + 1;
+  if (good >= interval) {
+    float grown = *scale * growth;
+    if (isfinite(grown)) *scale = grown;
+    good = 0;
+  }
+  *good_steps = good;
+}
+
+/* ---------------------------------------------------------------------------------
  * ZeRO-3 parameter gather: the arithmetic of the all-gather before forward (ZeRO
  * explainer, Chapter 02, ZeRO-3 item). The fp16 shards concatenate to the flat buffer;
  * layer l is the slice [off[l], off[l+1]) of it, copied to its own contiguous buffer.

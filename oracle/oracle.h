@@ -89,6 +89,14 @@ void oracle_step(int32_t nd, const uint16_t* const* contrib, int64_t n, int64_t 
                  float* gsum_work, float loss_scale, float clip, const oracle_hparams* hp,
                  int64_t t, oracle_scalars* out);
 
+/* Dynamic loss scaling after a step (mixed-precision practice; the pages name mixed
+ * precision but no scaler): on overflow the scale is multiplied by backoff and the count
+ * of good steps restarts; otherwise the count grows, and when it reaches interval the
+ * scale is multiplied by growth (unless that product is not finite) and the count
+ * restarts. fp32 multiplies. */
+void oracle_scaler_update(float* scale, int32_t* good_steps, int32_t overflow, float growth,
+                          float backoff, int32_t interval);
+
 /* ZeRO-3 parameter gather: dst[l][j] = flat[off[l] + j] for j < off[l+1] - off[l], where
  * flat is the concatenation of the nd shards of shard_len elements each. */
 void oracle_gather(int32_t nd, int64_t shard_len, const uint16_t* const* shards,

@@ -98,6 +98,11 @@ WORKLOADS = {
         Workload("flat_32m_nd8", cfg=5, n=33_554_432, nd=8, align=128, stage=2, r0=0, r1=8,
                  loss_scale=65536.0, grad_sigma=1e-3, clip=1.0, steps=3,
                  m_sigma=1e-3, v_sigma=1e-6),
+        # the 13B ZeRO-3 recipe at a tenth of the size (40 layers of 32.5M, 5.2 GB of shards
+        # and layers): a case for detailed profiler captures of the gather
+        Workload("zero3_1p3b_rank0_nd64", cfg=6, n=1_300_000_000, nd=64, align=8, stage=3,
+                 r0=0, r1=1, loss_scale=1024.0, grad_sigma=1e-3, clip=1.0, steps=5,
+                 layers=tuple(l * 32_500_000 for l in range(41))),
         # 13B, 40 layers of 325M, ZeRO-3: rank 0's step over S ~ 203M, then the gather of
         # all 64 fp16 shards into the 40 layer buffers
         Workload("zero3_13b_rank0_nd64", cfg=4, n=13_000_000_000, nd=64, align=8, stage=3, r0=0,
