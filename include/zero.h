@@ -191,6 +191,36 @@ int zero_memory_bytes(int64_t n_params, int32_t nd, int32_t align, int32_t stage
 int zero_profile_enable(zero_plan* plan, int32_t on);
 int zero_profile_read(zero_plan* plan, double* ms, int64_t* launches, int32_t reset);
 
+/* A shard step that allocates nothing. The paper has no counterpart: this is an interface
+ * variant of zero_shard_step for callers that cannot allocate device memory when they step
+ * (a framework that reserved all of HBM for its own pool at start-up and forbids later
+ * cudaMalloc calls, an allocator hook that must not re-enter its allocator, or a loop in
+ * which the device-wide synchronisation that cudaMalloc/cudaFree may cause is not
+ * acceptable). It needs no plan and runs the same reduce and update kernels.
+ *   nd: ranks, 1..ZERO_MAX_ND; n: span length, a multiple of 8, 8 <= n <=
+ *     ZERO_NOALLOC_MAX_SPAN; n_valid: real parameters at the start of the span (0..n);
+ *     n * nd^2 < 2^47;
+ *   grad_ptrs: host array of nd device pointers, fp16[n] each, 16-byte aligned;
+ *   master, exp_avg, exp_avg_sq: fp32[n]; param16: fp16[n]; device, 16-byte aligned;
+ *   step_counter: one int64 in device memory, the optimizer step counter t, read before
+ *     and written after the step (it stays unchanged when the step is skipped);
+ *   hp, loss_scale, clip: as for zero_plan_create and zero_shard_step.
+ * The caller passes every input and output. Scratch comes from one device array inside
+ * this library: ZERO_NOALLOC_MAX_SPAN fp32 values plus a control block of about 34 KiB
+ * (16.03 MiB), which every GPU that loads the library holds until the process exits. The
+ * first call on a device looks up that array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture. Every call shares the array
+ * and it keeps the last call's contents (the control word that must start at zero is
+ * cleared by each call), so calls whose work overlaps on the GPU race and give wrong
+ * results: order them on one stream or with events. Enqueued on stream; asynchronous.
+ * Errors: ZERO_EINVAL (including n > ZERO_NOALLOC_MAX_SPAN), ZERO_EALIGN, ZERO_ECUDA;
+ * nothing is launched on an error. */
+#define ZERO_NOALLOC_MAX_SPAN 4194304
+int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid, const void* const* grad_ptrs,
+                            float* master, float* exp_avg, float* exp_avg_sq, void* param16,
+                            int64_t* step_counter, const zero_adam_hparams* hp,
+                            float loss_scale, float clip, void* stream);
+
 /* Message of the calling thread's last error ("" if none). Valid until the thread's
  * next libzero call. */
 const char* zero_last_error(void);

@@ -24,6 +24,7 @@ ZERO_EDEVICE = -5
 ZERO_MAX_ND = 256
 ZERO_STATS_WORDS = 8
 ZERO_PROF_KINDS = 4
+ZERO_NOALLOC_MAX_SPAN = 4194304
 PROF_REDUCE, PROF_UPDATE, PROF_FINALIZE, PROF_GATHER = range(4)
 
 
@@ -73,6 +74,8 @@ _SIGS = {
     "zero_profile_enable": ([_P, _I32], ctypes.c_int),
     "zero_profile_read": ([_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64), _I32],
                           ctypes.c_int),
+    "zero_shard_step_noalloc": ([_I32, _I64, _I64, _PP, _P, _P, _P, _P, _P,
+                                 ctypes.POINTER(zero_adam_hparams), _F, _F, _P], ctypes.c_int),
     "zero_last_error": ([], ctypes.c_char_p),
 }
 _lib_handle = None
@@ -304,3 +307,17 @@ def zero_dist_step(plan: Plan, r0: int, r1: int, grads: Sequence, loss_scale: fl
     with torch.cuda.stream(s):
         dist.all_reduce(words, op=dist.ReduceOp.SUM, group=group)
     zero_shard_update(plan, r0, r1, loss_scale, clip, s)
+
+
+def zero_shard_step_noalloc(nd: int, n: int, n_valid: int, grads: Sequence, master, exp_avg,
+                            exp_avg_sq, param16, step_counter, hp: zero_adam_hparams | dict,
+                            loss_scale: float, clip: float, stream=None) -> None:
+    """The shard step without a plan and without allocating anything (see zero.h): for
+    callers that cannot allocate device memory when they step. ``step_counter`` is a
+    one-element int64 device tensor (or address) holding the optimizer step counter."""
+    if isinstance(hp, dict):
+        hp = zero_adam_hparams(**hp)
+    _check(_lib.zero_shard_step_noalloc(nd, n, n_valid, _ptrs(grads), _addr(master),
+                                        _addr(exp_avg), _addr(exp_avg_sq), _addr(param16),
+                                        _addr(step_counter), ctypes.byref(hp), loss_scale,
+                                        clip, _stream(stream)))

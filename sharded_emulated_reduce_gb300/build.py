@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libzero.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
-CU_SOURCES = ["step_kernels.cu", "gather_kernel.cu"]
+CU_SOURCES = ["step_kernels.cu", "gather_kernel.cu", "noalloc.cu"]
 CPP_SOURCES = ["plan.cpp"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "zero.h")]
 

@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/zero.h"
+#include "zero.h"
 
 namespace zero {
 
@@ -84,6 +84,9 @@ cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,
                             const HostHParams& hp, cudaStream_t s);
 cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherLaunch& p, cudaStream_t s);
+
+// Set the calling thread's zero_last_error() message; returns code.
+int set_error(int code, const char* msg);
 
 // Occupancy-derived persistent grid size of the gather for the current device.
 int gather_grid(int64_t tiles);

@@ -47,6 +47,11 @@ constexpr size_t kMaxPendingEvents = 1 << 16;
 
 }  // namespace
 
+int zero::set_error(int code, const char* msg) {
+  g_error = msg;
+  return code;
+}
+
 struct zero_plan {
   int64_t n = 0, np = 0, s = 0;
   int32_t nd = 0, stage = 0, align = 0;

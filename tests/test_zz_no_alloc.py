@@ -1,0 +1,78 @@
+"""The shard step that allocates nothing, checked against the plan-based step.
+
+Some callers cannot allocate device memory at the moment they run the optimizer step:
+their framework reserved all of HBM for its own pool at start-up, they run inside an
+allocator hook, or they cannot afford the device-wide synchronisation cudaMalloc and
+cudaFree may cause. zero_shard_step_noalloc serves them from a fixed scratch array
+inside the library. Here two calls in a row must leave the same state and step counter
+as zero_shard_step on identical inputs, within the tolerances of the other parity tests
+(1e-6 relative for master/m/v, one fp16 ulp for the parameters), and a span longer than
+the array must be refused with a clear error. The test stands alone: it needs nothing
+from the tests collected before it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import sharded_emulated_reduce_gb300 as z
+from synth import workloads as wl
+
+from parity import assert_p16_close, assert_state_close, f32, h16
+
+pytestmark = pytest.mark.gpu
+
+
+def test_noalloc_step_matches_plan_step_on_two_calls():
+    w = wl.Workload("noalloc", cfg=300, n=3_000_001, nd=8, align=8, stage=2, r0=0, r1=8,
+                    loss_scale=65536.0, grad_sigma=1e-3, clip=1.0, steps=2, m_sigma=1e-3,
+                    v_sigma=1e-6)
+    first, n_span, n_valid = w.span()
+    assert n_span <= z.ZERO_NOALLOC_MAX_SPAN
+    ref = wl.make_state(w)
+    mine = [t.clone() for t in ref[:4]]
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, 0, w.nd, *ref, 0)
+    counter = torch.zeros(1, dtype=torch.int64, device="cuda")
+    grads = [torch.empty(n_span, dtype=torch.float16, device="cuda") for _ in range(w.nd)]
+    for step in range(2):
+        wl.fill_grads(w, step, grads)
+        z.zero_shard_step(plan, 0, w.nd, grads, w.loss_scale, w.clip)
+        info = z.zero_step_result(plan)
+        z.zero_shard_step_noalloc(w.nd, n_span, n_valid, grads, *mine, counter, w.hparams(),
+                                  w.loss_scale, w.clip)
+        torch.cuda.synchronize()
+        assert info.skipped == 0
+        assert int(counter.item()) == info.step == step + 1
+        for name, a, b in zip(("master", "exp_avg", "exp_avg_sq"), mine[:3], ref[:3]):
+            assert_state_close(name, f32(a)[:n_valid], f32(b)[:n_valid])
+            assert np.array_equal(f32(a).view(np.uint32), f32(b).view(np.uint32))
+        assert_p16_close(h16(mine[3])[:n_valid], h16(ref[3])[:n_valid])
+        assert np.array_equal(h16(mine[3]), h16(ref[3]))
+    plan.close()
+
+
+def test_noalloc_skips_an_overflow_step_and_keeps_the_counter():
+    n, nd = 4096, 4
+    master = torch.zeros(n, device="cuda")
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    p16 = torch.zeros(n, dtype=torch.float16, device="cuda")
+    counter = torch.full((1,), 7, dtype=torch.int64, device="cuda")
+    grads = [torch.ones(n, dtype=torch.float16, device="cuda") for _ in range(nd)]
+    grads[2][100] = float("inf")
+    z.zero_shard_step_noalloc(nd, n, n, grads, master, m, v, p16, counter,
+                              dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0),
+                              1.0, 0.0)
+    torch.cuda.synchronize()
+    assert int(counter.item()) == 7
+    assert not master.any() and not m.any() and not v.any()
+
+
+def test_noalloc_refuses_spans_beyond_its_array():
+    fake = [0x10000 + 0x1000 * k for k in range(4)]
+    n = z.ZERO_NOALLOC_MAX_SPAN + 8
+    with pytest.raises(z.ZeroError) as ei:
+        z.zero_shard_step_noalloc(4, n, n, fake, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000,
+                                  dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                                       weight_decay=0.0), 1.0, 0.0)
+    assert ei.value.code == z.ZERO_EINVAL
+    assert "ZERO_NOALLOC_MAX_SPAN" in str(ei.value)
