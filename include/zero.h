@@ -24,7 +24,10 @@
  *
  * Conventions for every call:
  *   - Device memory (gradients, state, workspace, shards, layer buffers) is allocated
- *     and owned by the caller; the library never frees it. A plan owns only its host
+ *     and owned by the caller; the library never frees it. "Device pointer" means an
+ *     address the GPU can dereference: HBM, or pinned or registered host memory (on a
+ *     GB300 the kernels then read and write it over NVLink-C2C, which is how optimizer
+ *     state or fp16 shards can live in Grace memory — the offload variant of ZeRO). A plan owns only its host
  *     metadata, a small device scratch area (< 64 KiB, allocated by zero_plan_bind on
  *     the device current at that time, freed by zero_plan_destroy) and a few pinned
  *     host bytes.
@@ -66,7 +69,9 @@ typedef struct {
 typedef struct {
   int32_t overflow;   /* 1 if any summed gradient in the span was inf or nan          */
   int32_t skipped;    /* 1 if the update was not applied (overflow or status != 0)    */
-  int32_t status;     /* 0, or a device-side failure code (nothing was written)       */
+  int32_t status;     /* 0, or a device-side failure code: 2 = a bulk load of the
+                       * update did not arrive within its bounded wait (the update may be
+                       * partly applied; never expected on a healthy GPU)               */
   int32_t reserved;
   int64_t step;       /* optimizer step counter after the step                        */
   double global_norm; /* L2 norm of the unscaled summed gradient (+inf on overflow)   */
@@ -74,8 +79,31 @@ typedef struct {
   double clip_coef;   /* min(1, clip / (global_norm + 1e-6)), or 1 without clipping    */
   float scale;        /* fp32 factor applied to the summed gradient: clip_coef / loss_scale */
   float bc1, bc2;     /* fp32 bias corrections 1 - beta^step used by the update       */
-  float reserved2;
+  float loss_scale;   /* the loss scale the step's gradients carried                 */
 } zero_step_info;
+
+/* Dynamic loss scaling kept on the device (mixed-precision practice; the pages name
+ * mixed precision but give no scaling policy). After each step: on an overflow the
+ * scale is multiplied by backoff_factor and good_steps restarts at 0; otherwise
+ * good_steps grows by one, and when it reaches growth_interval the scale is multiplied
+ * by growth_factor (unless that product is not finite) and good_steps restarts. fp32
+ * multiplies. */
+typedef struct {
+  float scale;             /* current loss scale: finite, > 0                          */
+  int32_t good_steps;      /* applied steps since the scale last changed, >= 0         */
+  float growth_factor;     /* >= 1                                                     */
+  float backoff_factor;    /* in (0, 1]                                                */
+  int32_t growth_interval; /* >= 1 turns the scaler on; 0 turns it off                 */
+  int32_t reserved;
+} zero_loss_scaler;
+
+/* Everything a plan holds besides the caller's buffers: with the bound master, exp_avg,
+ * exp_avg_sq and param16 it is a complete checkpoint of a span (ZeRO explainer, Legacy:
+ * sharding multiplies failure domains, so each rank checkpoints its own partition). */
+typedef struct {
+  int64_t step;            /* optimizer step counter t                                 */
+  zero_loss_scaler scaler;
+} zero_plan_state;
 
 typedef struct zero_plan zero_plan; /* opaque */
 
@@ -122,7 +150,9 @@ int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float
  *   grad_ptrs: host array of nd device pointers; grad_ptrs[k] is rank k's fp16
  *     gradient for the span, n elements, 16-byte aligned. Element i of every rank
  *     belongs to flat index r0*S + i.
- *   loss_scale: finite and > 0; the summed gradient is divided by it.
+ *   loss_scale: finite and > 0; the summed gradient is divided by it. With the plan's
+ *     dynamic loss scaler on (zero_plan_set_scaler) it must be 0: the device scale is
+ *     used and then updated.
  *   clip: global-norm threshold; <= 0 disables clipping. Must be finite.
  * Computes, on the device, gsum = the fp32 sum of the nd contributions in rank order
  * 0..nd-1 (the reduce-scatter's arithmetic), the overflow flag and the norm over the
@@ -220,6 +250,25 @@ int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid, const void* 
                             float* master, float* exp_avg, float* exp_avg_sq, void* param16,
                             int64_t* step_counter, const zero_adam_hparams* hp,
                             float loss_scale, float clip, void* stream);
+
+/* Configure the plan's device-resident loss scaler (see zero_loss_scaler) after
+ * zero_plan_bind. While it is on, zero_shard_step and zero_shard_update must be given
+ * loss_scale = 0 and use the device scale instead; zero_loss_scale_ptr gives its address
+ * so that the caller can scale its loss on the device without a host round trip.
+ * Waits for the plan's last stream, then writes the state (synchronous). Errors:
+ * ZERO_EINVAL, ZERO_EUNBOUND, ZERO_ECUDA. */
+int zero_plan_set_scaler(zero_plan* plan, const zero_loss_scaler* scaler);
+
+/* Device address of the current loss scale (one fp32 value in the plan's scratch). Valid
+ * after zero_plan_bind and until zero_plan_destroy. Errors: ZERO_EINVAL, ZERO_EUNBOUND. */
+int zero_loss_scale_ptr(zero_plan* plan, float** dev_scale);
+
+/* Read (get) or restore (set) the plan's step counter and scaler, for checkpoints: saving
+ * the bound buffers and this state, then binding fresh buffers holding the saved bytes and
+ * restoring the state, continues the run bit for bit. Both wait for the plan's last
+ * stream (synchronous). Errors: ZERO_EINVAL, ZERO_EUNBOUND, ZERO_ECUDA. */
+int zero_plan_get_state(zero_plan* plan, zero_plan_state* out);
+int zero_plan_set_state(zero_plan* plan, const zero_plan_state* in);
 
 /* Message of the calling thread's last error ("" if none). Valid until the thread's
  * next libzero call. */

@@ -45,10 +45,26 @@ class zero_step_info(ctypes.Structure):
                 ("step", ctypes.c_int64), ("global_norm", ctypes.c_double),
                 ("sum_sq", ctypes.c_double), ("clip_coef", ctypes.c_double),
                 ("scale", ctypes.c_float), ("bc1", ctypes.c_float), ("bc2", ctypes.c_float),
-                ("reserved2", ctypes.c_float)]
+                ("loss_scale", ctypes.c_float)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_ if not k.startswith("reserved")}
+
+
+class zero_loss_scaler(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("good_steps", ctypes.c_int32),
+                ("growth_factor", ctypes.c_float), ("backoff_factor", ctypes.c_float),
+                ("growth_interval", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_ if not k.startswith("reserved")}
+
+
+class zero_plan_state(ctypes.Structure):
+    _fields_ = [("step", ctypes.c_int64), ("scaler", zero_loss_scaler)]
+
+    def as_dict(self) -> dict:
+        return {"step": self.step, "scaler": self.scaler.as_dict()}
 
 
 _P = ctypes.c_void_p
@@ -76,6 +92,10 @@ _SIGS = {
                           ctypes.c_int),
     "zero_shard_step_noalloc": ([_I32, _I64, _I64, _PP, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(zero_adam_hparams), _F, _F, _P], ctypes.c_int),
+    "zero_plan_set_scaler": ([_P, ctypes.POINTER(zero_loss_scaler)], ctypes.c_int),
+    "zero_loss_scale_ptr": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
+    "zero_plan_get_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
+    "zero_plan_set_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
     "zero_last_error": ([], ctypes.c_char_p),
 }
 _lib_handle = None
@@ -321,3 +341,103 @@ def zero_shard_step_noalloc(nd: int, n: int, n_valid: int, grads: Sequence, mast
                                         _addr(exp_avg), _addr(exp_avg_sq), _addr(param16),
                                         _addr(step_counter), ctypes.byref(hp), loss_scale,
                                         clip, _stream(stream)))
+
+
+# ------------------------------------------------------------------------------------
+# Dynamic loss scale and checkpoints
+
+def zero_plan_set_scaler(plan: Plan, scale: float = 65536.0, growth_factor: float = 2.0,
+                         backoff_factor: float = 0.5, growth_interval: int = 2000,
+                         good_steps: int = 0) -> None:
+    """Turn the device-resident loss scaler on (growth_interval >= 1) or off (0). While it
+    is on, pass loss_scale = 0 to the step calls."""
+    c = zero_loss_scaler(scale, good_steps, growth_factor, backoff_factor, growth_interval, 0)
+    _check(_lib.zero_plan_set_scaler(plan, ctypes.byref(c)))
+
+
+def zero_loss_scale_ptr(plan: Plan) -> int:
+    """Device address of the current fp32 loss scale."""
+    p = ctypes.c_void_p()
+    _check(_lib.zero_loss_scale_ptr(plan, ctypes.byref(p)))
+    return p.value
+
+
+def zero_plan_get_state(plan: Plan) -> zero_plan_state:
+    st = zero_plan_state()
+    _check(_lib.zero_plan_get_state(plan, ctypes.byref(st)))
+    return st
+
+
+def zero_plan_set_state(plan: Plan, state: zero_plan_state) -> None:
+    _check(_lib.zero_plan_set_state(plan, ctypes.byref(state)))
+
+
+def zero_checkpoint_save(path: str, plan: Plan, master, exp_avg, exp_avg_sq, param16) -> None:
+    """Write one span's checkpoint: the plan's state and the raw bytes of its four bound
+    buffers (torch tensors on the device), as an uncompressed .npz file."""
+    import numpy as np
+    st = zero_plan_get_state(plan)
+    arrays = {name: t.detach().contiguous().view(-1).view(torch_uint8()).cpu().numpy()
+              for name, t in (("master", master), ("exp_avg", exp_avg),
+                              ("exp_avg_sq", exp_avg_sq), ("param16", param16))}
+    sc = st.scaler
+    meta = np.array([st.step, sc.good_steps, sc.growth_interval], dtype=np.int64)
+    fmeta = np.array([sc.scale, sc.growth_factor, sc.backoff_factor], dtype=np.float32)
+    geom = np.array([plan.n_params, plan.nd, plan.stage, plan.align], dtype=np.int64)
+    with open(path, "wb") as f:
+        np.savez(f, meta=meta, fmeta=fmeta, geom=geom, **arrays)
+
+
+def zero_checkpoint_load(path: str, plan: Plan, master, exp_avg, exp_avg_sq, param16) -> None:
+    """Restore a checkpoint written by zero_checkpoint_save into the given device buffers
+    (already bound to ``plan``, same sizes) and the plan's state."""
+    import numpy as np
+    import torch
+    with np.load(path) as z_:
+        geom = [int(x) for x in z_["geom"]]
+        if geom != [plan.n_params, plan.nd, plan.stage, plan.align]:
+            raise ZeroError(ZERO_EINVAL, f"checkpoint is for plan {geom}")
+        for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq),
+                        ("param16", param16)):
+            raw = torch.from_numpy(z_[name].copy())
+            dst = t.view(-1).view(torch.uint8)
+            if raw.numel() != dst.numel():
+                raise ZeroError(ZERO_EINVAL, f"checkpoint {name} has {raw.numel()} bytes, "
+                                             f"buffer has {dst.numel()}")
+            dst.copy_(raw)
+        meta, fmeta = z_["meta"], z_["fmeta"]
+    torch.cuda.synchronize()
+    st = zero_plan_state()
+    st.step = int(meta[0])
+    st.scaler = zero_loss_scaler(float(fmeta[0]), int(meta[1]), float(fmeta[1]), float(fmeta[2]),
+                                 int(meta[2]), 0)
+    zero_plan_set_state(plan, st)
+
+
+def torch_uint8():
+    import torch
+    return torch.uint8
+
+
+# ------------------------------------------------------------------------------------
+# Layer-by-layer gather with completion events (ZeRO-3 prefetch)
+
+def zero_prefetch_layers(plan: Plan, layer_offsets: Sequence[int], shards: Sequence,
+                         layer_dst: Sequence, stream=None, first: int = 0,
+                         count: int | None = None) -> list:
+    """Gather layers ``first .. first+count-1`` one launch each on ``stream`` and return one
+    torch.cuda.Event per layer, recorded right after that layer's copy. A consumer stream
+    that waits on event l can start on layer l while later layers are still being
+    gathered: the "dynamic communication schedule" of the ZeRO method entry, in which the
+    all-gather of the next layers runs ahead of the work on the current one."""
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    n_layers = len(layer_offsets) - 1
+    last = n_layers if count is None else min(n_layers, first + count)
+    events = []
+    for l in range(first, last):
+        zero_gather_layers(plan, layer_offsets[l:l + 2], shards, [layer_dst[l]], s)
+        ev = torch.cuda.Event()
+        ev.record(s)
+        events.append(ev)
+    return events

@@ -18,6 +18,17 @@ struct DevScalars {
   int64_t step;  // step counter after this step
   double ss, norm, clip_coef;
   float s, omb1, omb2, bc1, bc2, decay, lr, beta1, beta2, eps;
+  float loss_scale;  // the scale this step's gradients carried
+  float pad2;
+};
+
+// Dynamic loss scale kept on the device; growth_interval <= 0 means disabled.
+struct DevScaler {
+  float scale;
+  int32_t good_steps;
+  float growth, backoff;
+  int32_t interval;
+  int32_t pad;
 };
 
 // One reduce CTA's statistics: the 128-bit sum of squares and the non-finite count.
@@ -31,6 +42,7 @@ struct DevPartial {
 struct DevScratch {
   long long stats[ZERO_STATS_WORDS];  // exchange buffer (see zero_shard_stats)
   DevScalars sc;
+  DevScaler scaler;
   long long step;       // optimizer step counter t
   unsigned int ticket;  // arrival counter of the reduce CTAs
   unsigned int pad;
@@ -77,7 +89,7 @@ struct GatherLaunch {
   int grid;
 };
 
-constexpr int64_t kGatherTile = 8192;  // elements per gather tile (16 KiB)
+constexpr int64_t kGatherTile = 32768;  // elements per gather tile (64 KiB)
 
 cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s);
 cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,

@@ -69,6 +69,8 @@ struct zero_plan {
   cudaStream_t last_stream = nullptr;
   bool stepped = false;
 
+  bool scaler_on = false;  // host mirror of the device scaler's on/off switch
+
   bool prof = false;
   std::vector<EventPair> free_events, pending;
   double prof_ms[ZERO_PROF_KINDS] = {0, 0, 0, 0};
@@ -122,9 +124,13 @@ int check_grads(const zero_plan* p, const void* const* grads) {
   return ZERO_OK;
 }
 
-int check_scalars(float loss_scale, float clip) {
-  if (!std::isfinite(loss_scale) || loss_scale <= 0.0f)
+int check_scalars(const zero_plan* p, float loss_scale, float clip) {
+  if (p->scaler_on) {
+    if (loss_scale != 0.0f)
+      return fail(ZERO_EINVAL, "the plan's dynamic loss scaler is on: pass loss_scale = 0");
+  } else if (!std::isfinite(loss_scale) || loss_scale <= 0.0f) {
     return fail(ZERO_EINVAL, "loss_scale must be finite and > 0 (got %g)", (double)loss_scale);
+  }
   if (!std::isfinite(clip)) return fail(ZERO_EINVAL, "clip must be finite (got %g)", (double)clip);
   return ZERO_OK;
 }
@@ -329,7 +335,7 @@ int zero_shard_step(zero_plan* p, int32_t r0, int32_t r1, const void* const* gra
   g_error.clear();
   int rc = check_span(p, r0, r1);
   if (!rc) rc = check_grads(p, grads);
-  if (!rc) rc = check_scalars(loss_scale, clip);
+  if (!rc) rc = check_scalars(p, loss_scale, clip);
   if (!rc) rc = check_bound(p, r0, r1);
   if (!rc) rc = check_device(p);
   if (rc) return rc;
@@ -370,7 +376,7 @@ int zero_shard_update(zero_plan* p, int32_t r0, int32_t r1, float loss_scale, fl
                       void* stream) {
   g_error.clear();
   int rc = check_span(p, r0, r1);
-  if (!rc) rc = check_scalars(loss_scale, clip);
+  if (!rc) rc = check_scalars(p, loss_scale, clip);
   if (!rc) rc = check_bound(p, r0, r1);
   if (!rc) rc = check_device(p);
   if (rc) return rc;
@@ -409,6 +415,7 @@ int zero_step_result(zero_plan* p, zero_step_info* out) {
   out->scale = sc.s;
   out->bc1 = sc.bc1;
   out->bc2 = sc.bc2;
+  out->loss_scale = sc.loss_scale;
   if (sc.status != 0) return fail(ZERO_EDEVICE, "device status %d", sc.status);
   return ZERO_OK;
 }
@@ -525,6 +532,102 @@ int zero_profile_read(zero_plan* p, double* ms, int64_t* launches, int32_t reset
     }
   }
   return ZERO_OK;
+}
+
+namespace {
+
+int check_scaler(const zero_loss_scaler* c) {
+  if (!c) return fail(ZERO_EINVAL, "scaler is NULL");
+  if (c->growth_interval < 0) return fail(ZERO_EINVAL, "growth_interval must be >= 0");
+  if (c->growth_interval == 0) return ZERO_OK;  // off: the other fields are not used
+  if (!std::isfinite(c->scale) || c->scale <= 0.0f)
+    return fail(ZERO_EINVAL, "scale must be finite and > 0");
+  if (c->good_steps < 0) return fail(ZERO_EINVAL, "good_steps must be >= 0");
+  if (!std::isfinite(c->growth_factor) || c->growth_factor < 1.0f)
+    return fail(ZERO_EINVAL, "growth_factor must be finite and >= 1");
+  if (!(c->backoff_factor > 0.0f) || c->backoff_factor > 1.0f)
+    return fail(ZERO_EINVAL, "backoff_factor must be in (0, 1]");
+  return ZERO_OK;
+}
+
+int sync_last(zero_plan* p) {
+  cudaError_t e = cudaStreamSynchronize(p->last_stream);
+  return e == cudaSuccess ? ZERO_OK : cuda_fail(e, "cudaStreamSynchronize");
+}
+
+int write_scaler(zero_plan* p, const zero_loss_scaler* c) {
+  zero::DevScaler d{};
+  if (c->growth_interval > 0) {
+    d.scale = c->scale;
+    d.good_steps = c->good_steps;
+    d.growth = c->growth_factor;
+    d.backoff = c->backoff_factor;
+    d.interval = c->growth_interval;
+  }
+  cudaError_t e = cudaMemcpy(&p->scratch->scaler, &d, sizeof d, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(scaler)");
+  p->scaler_on = c->growth_interval > 0;
+  return ZERO_OK;
+}
+
+}  // namespace
+
+int zero_plan_set_scaler(zero_plan* p, const zero_loss_scaler* c) {
+  g_error.clear();
+  if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+  int rc = check_scaler(c);
+  if (rc) return rc;
+  if (!p->bound) return fail(ZERO_EUNBOUND, "no state is bound to the plan");
+  rc = check_device(p);
+  if (!rc) rc = sync_last(p);
+  if (rc) return rc;
+  return write_scaler(p, c);
+}
+
+int zero_loss_scale_ptr(zero_plan* p, float** dev_scale) {
+  g_error.clear();
+  if (!p || !dev_scale) return fail(ZERO_EINVAL, "NULL argument");
+  if (!p->scratch) return fail(ZERO_EUNBOUND, "no state is bound to the plan");
+  *dev_scale = &p->scratch->scaler.scale;
+  return ZERO_OK;
+}
+
+int zero_plan_get_state(zero_plan* p, zero_plan_state* out) {
+  g_error.clear();
+  if (!p || !out) return fail(ZERO_EINVAL, "NULL argument");
+  if (!p->bound) return fail(ZERO_EUNBOUND, "no state is bound to the plan");
+  int rc = check_device(p);
+  if (!rc) rc = sync_last(p);
+  if (rc) return rc;
+  long long t = 0;
+  zero::DevScaler d{};
+  cudaError_t e = cudaMemcpy(&t, &p->scratch->step, sizeof t, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&d, &p->scratch->scaler, sizeof d, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(state)");
+  std::memset(out, 0, sizeof *out);
+  out->step = t;
+  out->scaler.scale = d.scale;
+  out->scaler.good_steps = d.good_steps;
+  out->scaler.growth_factor = d.growth;
+  out->scaler.backoff_factor = d.backoff;
+  out->scaler.growth_interval = d.interval > 0 ? d.interval : 0;
+  return ZERO_OK;
+}
+
+int zero_plan_set_state(zero_plan* p, const zero_plan_state* in) {
+  g_error.clear();
+  if (!p || !in) return fail(ZERO_EINVAL, "NULL argument");
+  if (in->step < 0) return fail(ZERO_EINVAL, "step must be >= 0");
+  int rc = check_scaler(&in->scaler);
+  if (rc) return rc;
+  if (!p->bound) return fail(ZERO_EUNBOUND, "no state is bound to the plan");
+  rc = check_device(p);
+  if (!rc) rc = sync_last(p);
+  if (rc) return rc;
+  long long t = in->step;
+  cudaError_t e = cudaMemcpy(&p->scratch->step, &t, sizeof t, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step)");
+  return write_scaler(p, &in->scaler);
 }
 
 const char* zero_last_error(void) { return g_error.c_str(); }

@@ -9,8 +9,9 @@
 //            non-finite count per CTA; the last CTA to finish combines them.
 //   update:  reads the sum and the fp32 master/m/v (16 B/param), writes master/m/v and
 //            the fp16 parameter (14 B/param).
-// Both kernels are persistent grid-stride loops over groups of 8 elements: every
-// buffer access is one 16-byte vector per thread, coalesced across the warp.
+// The reduce is a persistent grid-stride loop over groups of 8 elements, one 16-byte
+// vector per rank per thread, coalesced across the warp. The update streams tiles through
+// shared memory with the TMA engine's 1-D bulk copies (see k_update).
 //
 // Exactness: each summed gradient gsum is an integer multiple of 2^-24 (fp16 values
 // are, and an fp32 sum of them stays one), so k = gsum * 2^24 is an exact integer and
@@ -84,10 +85,16 @@ __device__ double u128_to_double(U128 a) {
 
 // The step's scalars from its statistics (one thread). Double arithmetic, each
 // operation rounded to nearest, then one rounding to fp32.
-__device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float loss_scale,
+__device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float loss_scale_arg,
                                 float clip, const HostHParams& hp) {
   DevScalars sc;
   const long long t = st->step;
+  // with the dynamic scaler on, the gradients carry the device-resident scale
+  DevScaler scaler = st->scaler;
+  const bool dynamic = scaler.interval > 0;
+  const float loss_scale = dynamic ? scaler.scale : loss_scale_arg;
+  sc.loss_scale = loss_scale;
+  sc.pad2 = 0.0f;
   sc.pad = 0;
   sc.status = 0;
   sc.ss = __dmul_rn(u128_to_double(ss), 0x1p-48);
@@ -120,12 +127,30 @@ __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float lo
   sc.eps = hp.eps;
   st->sc = sc;
   if (!sc.skipped) st->step = t + 1;
+  if (dynamic) {
+    // back off on overflow; grow after `interval` consecutive applied steps
+    if (sc.overflow) {
+      scaler.scale = __fmul_rn(scaler.scale, scaler.backoff);
+      scaler.good_steps = 0;
+    } else {
+      int good = scaler.good_steps + 1;
+      if (good >= scaler.interval) {
+        const float grown = __fmul_rn(scaler.scale, scaler.growth);
+        if (is_finite(grown)) scaler.scale = grown;
+        good = 0;
+      }
+      scaler.good_steps = good;
+    }
+    st->scaler = scaler;
+  }
 }
 
-// Sum (acc, bad) over the CTA; the result is valid in thread 0.
+// Sum (acc, bad) over a CTA of NT threads; the result is valid in thread 0.
+template <int NT>
 __device__ void block_reduce(U128& acc, long long& bad) {
-  __shared__ unsigned long long s_lo[kThreads / 32], s_hi[kThreads / 32];
-  __shared__ long long s_bad[kThreads / 32];
+  static_assert(NT % 32 == 0, "whole warps");
+  __shared__ unsigned long long s_lo[NT / 32], s_hi[NT / 32];
+  __shared__ long long s_bad[NT / 32];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const unsigned long long lo = __shfl_xor_sync(0xffffffffu, acc.lo, o);
@@ -144,7 +169,7 @@ __device__ void block_reduce(U128& acc, long long& bad) {
   if (threadIdx.x == 0) {
     U128 t{0, 0};
     long long b = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
       add128(t, s_lo[w], s_hi[w]);
       b += s_bad[w];
     }
@@ -167,10 +192,12 @@ struct ReduceArgs {
 };
 
 // Sum the contributions of group v in rank order. ND > 0 fixes the rank count at
-// compile time; ND == 0 reads it from the arguments.
+// compile time; ND == 0 reads it from the arguments. Up to 8 ranks all loads are issued
+// at once; beyond that they are issued 8 ranks at a time, which keeps the register count
+// (and so the number of resident warps) at the level that saturates HBM.
 template <int ND, int CAP>
 __device__ __forceinline__ void sum_group(const ReduceArgs<CAP>& a, long long v, float (&s)[8]) {
-  if constexpr (ND > 0 && ND <= 16) {
+  if constexpr (ND > 0 && ND <= 8) {
     uint4 w[ND];
 #pragma unroll
     for (int r = 0; r < ND; ++r) w[r] = __ldcs(reinterpret_cast<const uint4*>(a.g[r]) + v);
@@ -222,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Red
   }
 
   // CTA partial, then the last CTA to arrive combines all partials (no waiting).
-  block_reduce(acc, bad);
+  block_reduce<kThreads>(acc, bad);
   __shared__ int s_last;
   DevScratch* st = a.st;
   if (threadIdx.x == 0) {
@@ -243,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Red
     add128(tot, __ldcg(&p->lo), __ldcg(&p->hi));
     tb += __ldcg(&p->bad);
   }
-  block_reduce(tot, tb);
+  block_reduce<kThreads>(tot, tb);
   if (threadIdx.x == 0) {
     st->stats[0] = tb;
     st->stats[1] = (long long)(tot.lo & 0xffffffffull);
@@ -301,8 +328,83 @@ __device__ __forceinline__ unsigned pack_h2(float a, float b) {
   return *reinterpret_cast<const unsigned*>(&h);
 }
 
-__global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ UpdateArgs a) {
-  const DevScalars* scp = &a.st->sc;
+// ---- bulk-async helpers (sm_90+ PTX, used on sm_103a) ----------------------------------
+// 1-D bulk copies between global and shared memory run on the TMA engine: loads signal
+// an mbarrier with their byte count (complete_tx), stores are tracked as bulk groups.
+// Every wait on an mbarrier is bounded: on expiry the kernel records a status and stops.
+
+constexpr unsigned kWaitLimit = 1u << 22;  // try_wait polls before a wait is abandoned
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
+               "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  const uint32_t a = smem_addr(b);
+  for (unsigned i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst_smem)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_addr(src_smem)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_to_async_proxy() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- the update kernel -------------------------------------------------------------------
+// One CTA of 512 threads per SM walks tiles of kUpdTile parameters. For each tile the TMA
+// engine brings the fp32 sum and master/m/v into a 3-stage shared-memory ring; the threads
+// update 4 parameters each into a double-buffered output area, and one thread sends the
+// new master/m/v and fp16 parameters back with bulk stores and refills the freed stage.
+// Loads for the next tiles stay in flight while the division-heavy arithmetic runs, so
+// the kernel streams at the HBM copy rate. Parameters past the last multiple of 8 (at most
+// 7, at the end of the real ones) are updated one by one after the tiles.
+constexpr int kUpdTile = 2048;
+constexpr int kUpdStages = 3;
+constexpr int kUpdThreads = 512;
+constexpr size_t kUpdIn = (size_t)kUpdStages * 4 * kUpdTile * sizeof(float);
+constexpr size_t kUpdOutF = (size_t)2 * 3 * kUpdTile * sizeof(float);
+constexpr size_t kUpdOutH = (size_t)2 * kUpdTile * sizeof(uint16_t);
+constexpr size_t kUpdSmem = kUpdIn + kUpdOutF + kUpdOutH + kUpdStages * sizeof(uint64_t);
+static_assert(kUpdThreads * 4 == kUpdTile, "each thread updates 4 parameters per tile");
+constexpr int32_t kStatusUpdateWait = 2;  // a bulk load did not arrive in time
+
+__global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant__ UpdateArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* in = reinterpret_cast<float*>(smem);
+  float* outf = reinterpret_cast<float*>(smem + kUpdIn);
+  uint16_t* outh = reinterpret_cast<uint16_t*>(smem + kUpdIn + kUpdOutF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kUpdIn + kUpdOutF + kUpdOutH);
+  DevScratch* st = a.st;
+  const DevScalars* scp = &st->sc;
   if (scp->skipped) return;  // overflow: the state keeps its bits
   Sc c;
   c.s = scp->s;
@@ -316,48 +418,98 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Upd
   c.decay = scp->decay;
   c.lr = scp->lr;
 
-  const long long n_full = a.n_valid >> 3;  // groups made only of real parameters
-  const long long stride = (long long)gridDim.x * kThreads;
-  const float4* g4 = reinterpret_cast<const float4*>(a.gsum);
-  float4* p4 = reinterpret_cast<float4*>(a.master);
-  float4* m4 = reinterpret_cast<float4*>(a.m);
-  float4* v4 = reinterpret_cast<float4*>(a.v);
-  uint4* h4 = reinterpret_cast<uint4*>(a.p16);
-  for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < n_full; i += stride) {
-    const float4 ga = __ldcs(g4 + 2 * i), gb = __ldcs(g4 + 2 * i + 1);
-    const float4 pa = __ldcs(p4 + 2 * i), pb = __ldcs(p4 + 2 * i + 1);
-    float4 ma = __ldcs(m4 + 2 * i), mb = __ldcs(m4 + 2 * i + 1);
-    float4 va = __ldcs(v4 + 2 * i), vb = __ldcs(v4 + 2 * i + 1);
-    float4 qa, qb;
-    qa.x = adam_elem(ga.x, pa.x, ma.x, va.x, c);
-    qa.y = adam_elem(ga.y, pa.y, ma.y, va.y, c);
-    qa.z = adam_elem(ga.z, pa.z, ma.z, va.z, c);
-    qa.w = adam_elem(ga.w, pa.w, ma.w, va.w, c);
-    qb.x = adam_elem(gb.x, pb.x, mb.x, vb.x, c);
-    qb.y = adam_elem(gb.y, pb.y, mb.y, vb.y, c);
-    qb.z = adam_elem(gb.z, pb.z, mb.z, vb.z, c);
-    qb.w = adam_elem(gb.w, pb.w, mb.w, vb.w, c);
-    __stcs(p4 + 2 * i, qa);
-    __stcs(p4 + 2 * i + 1, qb);
-    __stcs(m4 + 2 * i, ma);
-    __stcs(m4 + 2 * i + 1, mb);
-    __stcs(v4 + 2 * i, va);
-    __stcs(v4 + 2 * i + 1, vb);
-    __stcs(h4 + i, make_uint4(pack_h2(qa.x, qa.y), pack_h2(qa.z, qa.w), pack_h2(qb.x, qb.y),
-                              pack_h2(qb.z, qb.w)));
+  const long long n8 = a.n_valid & ~7ll;  // tiles cover whole groups of 8 (16-byte rule)
+  const long long ntiles = (n8 + kUpdTile - 1) / kUpdTile;
+  const int tid = threadIdx.x;
+  auto tile_of = [&](long long k) { return (long long)blockIdx.x + k * gridDim.x; };
+  auto tile_len = [&](long long t) {
+    const long long left = n8 - t * kUpdTile;
+    return left < kUpdTile ? left : (long long)kUpdTile;
+  };
+  auto issue = [&](long long k, int s) {  // one thread: load tile k into stage s
+    const long long t = tile_of(k);
+    const long long base = t * kUpdTile;
+    const uint32_t bytes = (uint32_t)(tile_len(t) * sizeof(float));
+    float* d = in + (size_t)s * 4 * kUpdTile;
+    mbar_expect_tx(&full[s], 4 * bytes);
+    bulk_load(d, a.gsum + base, bytes, &full[s]);
+    bulk_load(d + kUpdTile, a.master + base, bytes, &full[s]);
+    bulk_load(d + 2 * kUpdTile, a.m + base, bytes, &full[s]);
+    bulk_load(d + 3 * kUpdTile, a.v + base, bytes, &full[s]);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kUpdStages; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
   }
-  // The group that holds the end of the real parameters: element-wise, real ones only.
-  const long long rem = a.n_valid & 7;
-  if (rem != 0 && blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
-    const long long b = n_full * 8;
-    for (long long j = b; j < b + rem; ++j) {
-      float m = a.m[j], v = a.v[j];
-      const float p = adam_elem(a.gsum[j], a.master[j], m, v, c);
-      a.master[j] = p;
-      a.m[j] = m;
-      a.v[j] = v;
+  __syncthreads();
+  if (tid == 0)
+    for (int s = 0; s < kUpdStages; ++s)
+      if (tile_of(s) < ntiles) issue(s, s);
+
+  bool ok = true;
+  long long k = 0;
+  for (; tile_of(k) < ntiles; ++k) {
+    const int s = (int)(k % kUpdStages);
+    const int ob = (int)(k & 1);
+    const long long t = tile_of(k);
+    const long long base = t * kUpdTile;
+    const long long cnt = tile_len(t);
+    const bool arrived = mbar_wait(&full[s], (uint32_t)((k / kUpdStages) & 1));
+    if (tid == 0) bulk_wait_read_all_but_one();  // tile k-2's stores have read buffer ob
+    if (!__syncthreads_and(arrived)) {
+      ok = false;
+      break;
+    }
+    const int j = tid * 4;
+    if (j < cnt) {
+      const float* d = in + (size_t)s * 4 * kUpdTile;
+      const float4 g = *reinterpret_cast<const float4*>(d + j);
+      const float4 p = *reinterpret_cast<const float4*>(d + kUpdTile + j);
+      float4 m = *reinterpret_cast<const float4*>(d + 2 * kUpdTile + j);
+      float4 v = *reinterpret_cast<const float4*>(d + 3 * kUpdTile + j);
+      float4 q;
+      q.x = adam_elem(g.x, p.x, m.x, v.x, c);
+      q.y = adam_elem(g.y, p.y, m.y, v.y, c);
+      q.z = adam_elem(g.z, p.z, m.z, v.z, c);
+      q.w = adam_elem(g.w, p.w, m.w, v.w, c);
+      float* o = outf + (size_t)ob * 3 * kUpdTile;
+      *reinterpret_cast<float4*>(o + j) = q;
+      *reinterpret_cast<float4*>(o + kUpdTile + j) = m;
+      *reinterpret_cast<float4*>(o + 2 * kUpdTile + j) = v;
+      *reinterpret_cast<uint2*>(outh + (size_t)ob * kUpdTile + j) =
+          make_uint2(pack_h2(q.x, q.y), pack_h2(q.z, q.w));
+    }
+    fence_to_async_proxy();  // shared-memory writes become visible to the bulk stores
+    __syncthreads();         // every thread is done with stage s and buffer ob
+    if (tid == 0) {
+      const float* o = outf + (size_t)ob * 3 * kUpdTile;
+      const uint32_t bytes = (uint32_t)(cnt * sizeof(float));
+      bulk_store(a.master + base, o, bytes);
+      bulk_store(a.m + base, o + kUpdTile, bytes);
+      bulk_store(a.v + base, o + 2 * kUpdTile, bytes);
+      bulk_store(a.p16 + base, outh + (size_t)ob * kUpdTile, (uint32_t)(cnt * sizeof(uint16_t)));
+      bulk_commit();
+      if (tile_of(k + kUpdStages) < ntiles) issue(k + kUpdStages, s);
+    }
+  }
+  if (!ok) {
+    if (tid == 0) atomicExch(&st->sc.status, kStatusUpdateWait);
+    // let the loads already issued land before this CTA's shared memory is released
+    for (long long q = k; q < k + kUpdStages && tile_of(q) < ntiles; ++q)
+      mbar_wait(&full[(int)(q % kUpdStages)], (uint32_t)((q / kUpdStages) & 1));
+  }
+  if (tid == 0) bulk_wait_all();
+  const long long rem = a.n_valid - n8;
+  if (ok && rem != 0 && blockIdx.x == gridDim.x - 1 && tid == 0) {
+    for (long long i = n8; i < a.n_valid; ++i) {
+      float m = a.m[i], v = a.v[i];
+      const float p = adam_elem(a.gsum[i], a.master[i], m, v, c);
+      a.master[i] = p;
+      a.m[i] = m;
+      a.v[i] = v;
       const __half h = __float2half_rn(p);
-      a.p16[j] = *reinterpret_cast<const uint16_t*>(&h);
+      a.p16[i] = *reinterpret_cast<const uint16_t*>(&h);
     }
   }
 }
@@ -434,9 +586,22 @@ cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s) {
   a.p16 = static_cast<uint16_t*>(p.param16);
   a.n_valid = p.n_valid;
   a.st = p.scratch;
-  int grid = occupancy_grid(k_update, (p.n_valid + 7) / 8);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {};
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(k_update, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kUpdSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long tiles = ((p.n_valid & ~7ll) + kUpdTile - 1) / kUpdTile;
+  long long grid = tiles < sms ? tiles : sms;  // one CTA per SM, persistent
+  if (grid < 1) grid = 1;
   if (p.grid > 0 && p.grid < grid) grid = p.grid;
-  k_update<<<grid, kThreads, 0, s>>>(a);
+  k_update<<<(int)grid, kUpdThreads, kUpdSmem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -145,3 +145,20 @@ def test_destroyed_plan_is_refused_by_the_binding():
     p.close()
     with pytest.raises(Exception, match="destroyed"):
         z.zero_plan_layout(p)
+
+
+def test_scaler_and_state_calls_validate_before_touching_the_device():
+    with z.zero_plan_create(100, 4, 2, 8, HP) as p:
+        for kw in [dict(scale=0.0, growth_interval=10), dict(scale=float("inf"), growth_interval=1),
+                   dict(growth_factor=0.5, growth_interval=1), dict(backoff_factor=0.0, growth_interval=1),
+                   dict(backoff_factor=1.5, growth_interval=1), dict(growth_interval=-1),
+                   dict(good_steps=-1, growth_interval=5)]:
+            expect(z.ZERO_EINVAL, lambda: z.zero_plan_set_scaler(p, **kw))
+        expect(z.ZERO_EUNBOUND, lambda: z.zero_plan_set_scaler(p, growth_interval=100))
+        expect(z.ZERO_EUNBOUND, z.zero_loss_scale_ptr, p)
+        expect(z.ZERO_EUNBOUND, z.zero_plan_get_state, p)
+        st = z.zero_plan_state()
+        st.step = -1
+        expect(z.ZERO_EINVAL, z.zero_plan_set_state, p, st)
+        st.step = 3
+        expect(z.ZERO_EUNBOUND, z.zero_plan_set_state, p, st)

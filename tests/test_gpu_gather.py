@@ -62,3 +62,30 @@ def test_many_segments_cross_the_per_launch_table():
     n, nd = 300 * 8 * 64, 64
     offsets = list(range(0, n + 1, n // 300))
     run_gather(n, nd, 8, offsets)
+
+
+def test_prefetch_layers_with_per_layer_events():
+    # producer stream gathers layer by layer; a consumer stream waits on each layer's
+    # event and reads it (sum of its bits) while later layers are still being gathered
+    n, nd = 4_000_000, 16
+    np_, s = oracle.partition(n, nd, 8)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    shards = [torch.randint(-30000, 30000, (s,), dtype=torch.int16, device="cuda", generator=g)
+              for _ in range(nd)]
+    offs = [l * 400_000 for l in range(11)]
+    dst = [torch.empty(offs[l + 1] - offs[l], dtype=torch.int16, device="cuda") for l in range(10)]
+    plan = z.zero_plan_create(n, nd, 3, 8, HP)
+    producer, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    events = z.zero_prefetch_layers(plan, offs, shards, dst, producer)
+    sums = []
+    for l, ev in enumerate(events):
+        consumer.wait_event(ev)
+        with torch.cuda.stream(consumer):
+            sums.append(dst[l].to(torch.int64).sum())
+    torch.cuda.synchronize()
+    exp = oracle.gather([h16(x) for x in shards], s, offs)
+    for l in range(10):
+        assert np.array_equal(h16(dst[l]), exp[l])
+        assert sums[l].item() == int(exp[l].view(np.int16).astype(np.int64).sum())
+    plan.close()
