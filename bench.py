@@ -388,24 +388,34 @@ def run_ours(args, w0):
     return 0
 
 
-def load_traffic(kernel: str, w):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the same
-    kernel source and workload; None otherwise."""
+KERNEL_SOURCES = ("step_kernels.cu", "gather_kernel.cu", "bulk_async.h", "internal.h")
+
+
+def kernel_source_hash() -> str:
+    """Short hash of the kernel sources; a committed traffic figure is used only if it was
+    captured on exactly these sources."""
     import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sharded_emulated_reduce_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str, w):
+    """Per-launch DRAM bytes (read + write) of `kernel` on workload `w` from the committed
+    ncu summary (profiles/ncu_traffic.json), if it was captured on the current kernel
+    sources; None otherwise."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    src = os.path.join(ROOT, "sharded_emulated_reduce_gb300", "csrc", "step_kernels.cu")
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    ent = d.get(w.name, {}).get(kernel)
-    if not ent or ent.get("source_sha256_16") != h:
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
-    return ent.get("dram_bytes_per_launch")
-
+    ent = d.get("workloads", {}).get(w.name, {}).get(kernel)
+    return None if not ent else ent.get("dram_bytes_per_launch")
 
 def run_gather(args, w):
     """Time the ZeRO-3 gather of all Nd fp16 shards into the workload's layer buffers."""
@@ -464,7 +474,8 @@ def run_gather(args, w):
         "e2e": None, "gpu_launches": int(kl[z.PROF_GATHER]),
         "roofline": {"bound": "hbm", "kernel": "gather", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": None, "alg_bytes_per_launch": alg, "avg_launch_ms": avg},
+                     "traffic": load_traffic("gather", w), "alg_bytes_per_launch": alg,
+                     "avg_launch_ms": avg},
         "cpu_baseline": None, "clocks": clk,
     }
     print(json.dumps(line))

@@ -198,9 +198,17 @@ int zero_step_result(zero_plan* plan, zero_step_info* out);
  *   layer_dst: host array of n_layers device pointers (2-byte aligned; may be NULL for
  *     an empty layer). Destinations must not overlap the shards or each other.
  * For ZeRO-1/2 the parameter all-gather is this call with one layer [0, n_params).
- * Enqueued on stream. Errors: ZERO_EINVAL, ZERO_ECUDA. */
+ * Enqueued on stream. The first call on a plan that was never bound allocates the
+ * plan's small device scratch (which holds the gather's status word) on the current
+ * device. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
 int zero_gather_layers(zero_plan* plan, const int64_t* layer_offsets, int32_t n_layers,
                        const void* const* shard_ptrs, void* const* layer_dst, void* stream);
+
+/* Wait for the plan's last gather and report whether it finished: *status is 0, or 4 if a
+ * bulk copy did not arrive within its bounded wait and the gather stopped early (never
+ * expected on a healthy GPU; the status is then cleared and ZERO_EDEVICE returned).
+ * Errors: ZERO_EINVAL, ZERO_ECUDA, ZERO_EDEVICE. */
+int zero_gather_status(zero_plan* plan, int32_t* status);
 
 /* Per-rank model-state bytes (ZeRO explainer, "The 16 Bytes per Parameter Audit",
  * Chapter 02 and the stage table): 2 B fp16 parameter + 2 B fp16 gradient + 12 B of
@@ -269,6 +277,15 @@ int zero_loss_scale_ptr(zero_plan* plan, float** dev_scale);
  * stream (synchronous). Errors: ZERO_EINVAL, ZERO_EUNBOUND, ZERO_ECUDA. */
 int zero_plan_get_state(zero_plan* plan, zero_plan_state* out);
 int zero_plan_set_state(zero_plan* plan, const zero_plan_state* in);
+
+/* Self-test of the bounded waits the bulk-copy kernels use (the pages have no
+ * counterpart; this checks the library's own failure path). A one-warp kernel waits on a
+ * shared-memory barrier that nothing completes, polling at most `polls` times (1..2^24,
+ * each poll suspended at most 1 us, the whole wait at most about 2 s), and records that it
+ * gave up; *expired receives 1 when the wait expired as it must, 0 if it (wrongly)
+ * completed. Synchronises the device; the context stays usable. Errors: ZERO_EINVAL,
+ * ZERO_ECUDA. */
+int zero_selftest_wait(uint32_t polls, int32_t* expired);
 
 /* Message of the calling thread's last error ("" if none). Valid until the thread's
  * next libzero call. */

@@ -87,6 +87,7 @@ _SIGS = {
     "zero_step_result": ([_P, ctypes.POINTER(zero_step_info)], ctypes.c_int),
     "zero_gather_layers": ([_P, ctypes.POINTER(_I64), _I32, _PP, _PP, _P], ctypes.c_int),
     "zero_memory_bytes": ([_I64, _I32, _I32, _I32, ctypes.POINTER(_I64)], ctypes.c_int),
+    "zero_gather_status": ([_P, ctypes.POINTER(_I32)], ctypes.c_int),
     "zero_profile_enable": ([_P, _I32], ctypes.c_int),
     "zero_profile_read": ([_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64), _I32],
                           ctypes.c_int),
@@ -96,6 +97,7 @@ _SIGS = {
     "zero_loss_scale_ptr": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
     "zero_plan_get_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
     "zero_plan_set_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
+    "zero_selftest_wait": ([ctypes.c_uint32, ctypes.POINTER(_I32)], ctypes.c_int),
     "zero_last_error": ([], ctypes.c_char_p),
 }
 _lib_handle = None
@@ -256,6 +258,13 @@ def zero_gather_layers(plan: Plan, layer_offsets: Sequence[int], shards: Sequenc
     offs = (_I64 * len(layer_offsets))(*[int(x) for x in layer_offsets])
     _check(_lib.zero_gather_layers(plan, offs, n_layers, _ptrs(shards), _ptrs(layer_dst),
                                    _stream(stream)))
+
+
+def zero_gather_status(plan: Plan) -> int:
+    """Wait for the plan's last gather; 0 if it finished (raises ZeroError otherwise)."""
+    st = _I32()
+    _check(_lib.zero_gather_status(plan, ctypes.byref(st)))
+    return st.value
 
 
 def zero_memory_bytes(n_params: int, nd: int, align: int, stage: int) -> int:
@@ -441,3 +450,10 @@ def zero_prefetch_layers(plan: Plan, layer_offsets: Sequence[int], shards: Seque
         ev.record(s)
         events.append(ev)
     return events
+
+
+def zero_selftest_wait(polls: int = 4096) -> int:
+    """Run the bounded-wait self-test; 1 means the wait expired and was reported."""
+    out = _I32()
+    _check(_lib.zero_selftest_wait(polls, ctypes.byref(out)))
+    return out.value

@@ -18,9 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libzero.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
-CU_SOURCES = ["step_kernels.cu", "gather_kernel.cu", "noalloc.cu"]
+CU_SOURCES = ["step_kernels.cu", "gather_kernel.cu", "noalloc.cu", "selftest.cu"]
 CPP_SOURCES = ["plan.cpp"]
-HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "zero.h")]
+HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "bulk_async.h"),
+           os.path.join(ROOT, "include", "zero.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # --fmad=false: no multiply-add contraction anywhere, so every fp32/fp64 operation is

@@ -44,8 +44,8 @@ struct DevScratch {
   DevScalars sc;
   DevScaler scaler;
   long long step;       // optimizer step counter t
-  unsigned int ticket;  // arrival counter of the reduce CTAs
-  unsigned int pad;
+  unsigned int ticket;    // arrival counter of the reduce CTAs
+  int32_t gather_status;  // 0, or kStatusGatherWait after a gather wait expired
   DevPartial partials[kMaxPartialBlocks];
 };
 
@@ -87,9 +87,11 @@ struct GatherLaunch {
   int nseg;
   int64_t tiles;       // total tiles over all segments
   int grid;
+  int32_t* status;     // set to kStatusGatherWait if a bounded wait expires
 };
 
 constexpr int64_t kGatherTile = 32768;  // elements per gather tile (64 KiB)
+constexpr int32_t kStatusGatherWait = 4;
 
 cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s);
 cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,

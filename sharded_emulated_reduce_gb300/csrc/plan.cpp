@@ -66,7 +66,8 @@ struct zero_plan {
   int device = -1;
   DevScratch* scratch = nullptr;
   zero::DevScalars* host_sc = nullptr;  // pinned
-  cudaStream_t last_stream = nullptr;
+  cudaStream_t last_stream = nullptr;    // stream of the last step (zero_step_result)
+  cudaStream_t gather_stream = nullptr;  // stream of the last gather (zero_gather_status)
   bool stepped = false;
 
   bool scaler_on = false;  // host mirror of the device scaler's on/off switch
@@ -157,6 +158,29 @@ void prof_end(zero_plan* p, cudaStream_t s, EventPair* ev, int kind) {
   cudaEventRecord(ev->stop, s);
   ev->kind = kind;
   p->pending.push_back(*ev);
+}
+
+// The plan's device scratch and pinned result buffer, allocated once on `dev`.
+int ensure_scratch(zero_plan* p, int dev) {
+  if (p->scratch) return ZERO_OK;
+  DevScratch* sc = nullptr;
+  cudaError_t e = cudaMalloc(&sc, sizeof(DevScratch));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(scratch)");
+  e = cudaMemset(sc, 0, sizeof(DevScratch));
+  if (e != cudaSuccess) {
+    cudaFree(sc);
+    return cuda_fail(e, "cudaMemset(scratch)");
+  }
+  zero::DevScalars* hs = nullptr;
+  e = cudaMallocHost(&hs, sizeof(zero::DevScalars));
+  if (e != cudaSuccess) {
+    cudaFree(sc);
+    return cuda_fail(e, "cudaMallocHost");
+  }
+  p->scratch = sc;
+  p->host_sc = hs;
+  p->device = dev;
+  return ZERO_OK;
 }
 
 int64_t n_valid_of_span(const zero_plan* p) {
@@ -296,25 +320,8 @@ int zero_plan_bind(zero_plan* p, int32_t r0, int32_t r1, float* master, float* e
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (p->scratch && dev != p->device)
     return fail(ZERO_EINVAL, "plan was bound on device %d; current device is %d", p->device, dev);
-  if (!p->scratch) {
-    DevScratch* sc = nullptr;
-    e = cudaMalloc(&sc, sizeof(DevScratch));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(scratch)");
-    e = cudaMemset(sc, 0, sizeof(DevScratch));
-    if (e != cudaSuccess) {
-      cudaFree(sc);
-      return cuda_fail(e, "cudaMemset(scratch)");
-    }
-    zero::DevScalars* hs = nullptr;
-    e = cudaMallocHost(&hs, sizeof(zero::DevScalars));
-    if (e != cudaSuccess) {
-      cudaFree(sc);
-      return cuda_fail(e, "cudaMallocHost");
-    }
-    p->scratch = sc;
-    p->host_sc = hs;
-    p->device = dev;
-  }
+  rc = ensure_scratch(p, dev);
+  if (rc) return rc;
   long long t = initial_step;
   e = cudaMemcpy(&p->scratch->step, &t, sizeof t, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(step)");
@@ -448,6 +455,8 @@ int zero_gather_layers(zero_plan* p, const int64_t* offs, int32_t n_layers,
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (p->device >= 0 && dev != p->device)
     return fail(ZERO_EINVAL, "current device %d differs from the plan's device %d", dev, p->device);
+  int rc0 = ensure_scratch(p, dev);  // holds the gather's status word
+  if (rc0) return rc0;
 
   // Cut each layer at shard boundaries; number the tiles of all segments in order.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -455,6 +464,7 @@ int zero_gather_layers(zero_plan* p, const int64_t* offs, int32_t n_layers,
   gl.nseg = 0;
   gl.tiles = 0;
   gl.grid = 0;
+  gl.status = &p->scratch->gather_status;
   auto flush = [&]() -> int {
     if (gl.nseg == 0) return ZERO_OK;
     EventPair ev;
@@ -484,7 +494,29 @@ int zero_gather_layers(zero_plan* p, const int64_t* offs, int32_t n_layers,
       gl.tiles += (sg.len + zero::kGatherTile - 1) / zero::kGatherTile;
     }
   }
-  return flush();
+  rc0 = flush();
+  if (!rc0) p->gather_stream = s;
+  return rc0;
+}
+
+int zero_gather_status(zero_plan* p, int32_t* status) {
+  g_error.clear();
+  if (!p || !status) return fail(ZERO_EINVAL, "NULL argument");
+  if (!p->scratch) {
+    *status = 0;  // no gather has run
+    return ZERO_OK;
+  }
+  int rc = check_device(p);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(p->gather_stream);
+  int32_t st = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpy(&st, &p->scratch->gather_status, sizeof st, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && st != 0) e = cudaMemset(&p->scratch->gather_status, 0, sizeof st);
+  if (e != cudaSuccess) return cuda_fail(e, "gather status");
+  *status = st;
+  if (st != 0) return fail(ZERO_EDEVICE, "a gather stopped early (status %d)", st);
+  return ZERO_OK;
 }
 
 int zero_memory_bytes(int64_t n, int32_t nd, int32_t align, int32_t stage, int64_t* out) {

@@ -22,6 +22,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include "bulk_async.h"
 #include "internal.h"
 
 namespace zero {
@@ -328,57 +329,6 @@ __device__ __forceinline__ unsigned pack_h2(float a, float b) {
   return *reinterpret_cast<const unsigned*>(&h);
 }
 
-// ---- bulk-async helpers (sm_90+ PTX, used on sm_103a) ----------------------------------
-// 1-D bulk copies between global and shared memory run on the TMA engine: loads signal
-// an mbarrier with their byte count (complete_tx), stores are tracked as bulk groups.
-// Every wait on an mbarrier is bounded: on expiry the kernel records a status and stops.
-
-constexpr unsigned kWaitLimit = 1u << 22;  // try_wait polls before a wait is abandoned
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
-               "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
-  const uint32_t a = smem_addr(b);
-  for (unsigned i = 0; i < kWaitLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done) : "r"(a), "r"(parity) : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_addr(dst_smem)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-               "r"(smem_addr(src_smem)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all_but_one() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_to_async_proxy() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---- the update kernel -------------------------------------------------------------------
 // One CTA of 512 threads per SM walks tiles of kUpdTile parameters. For each tile the TMA
 // engine brings the fp32 sum and master/m/v into a 3-stage shared-memory ring; the threads
@@ -514,20 +464,39 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
   }
 }
 
-template <typename K>
-int occupancy_grid(K kernel, long long work_items) {
-  static thread_local int cached_dev = -1;
-  static thread_local int sms = 0;
+constexpr int kMaxDevices = 64;
+
+// SM count of the current device, looked up once per device.
+int sm_count(int* dev_out) {
+  static int sms[kMaxDevices] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev != cached_dev) {
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cached_dev = dev;
+  if (dev_out) *dev_out = dev;
+  if (dev < 0 || dev >= kMaxDevices) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
   }
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
-  if (per_sm < 1) per_sm = 1;
-  long long g = (long long)sms * per_sm;
+  if (sms[dev] == 0) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev];
+}
+
+// Persistent grid for `kernel`: SMs x resident CTAs per SM, capped by the CTAs the work
+// needs. `per_sm` is the caller's per-device cache for this kernel (one static table per
+// launcher instantiation, because kernels of the same signature differ in occupancy).
+template <typename K>
+int occupancy_grid(K kernel, long long work_items, int (&per_sm)[kMaxDevices]) {
+  int dev = 0;
+  const int sms = sm_count(&dev);
+  int occ = 0;
+  if (dev >= 0 && dev < kMaxDevices && per_sm[dev] > 0) {
+    occ = per_sm[dev];
+  } else {
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+    if (occ < 1) occ = 1;
+    if (dev >= 0 && dev < kMaxDevices) per_sm[dev] = occ;
+  }
+  long long g = (long long)sms * occ;
   const long long need = (work_items + kThreads - 1) / kThreads;
   if (g > need) g = need;
   if (g < 1) g = 1;
@@ -547,7 +516,8 @@ cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s) {
   a.hp = p.hp;
   a.nd = p.nd;
   a.finalize = p.finalize ? 1 : 0;
-  int grid = occupancy_grid(k_reduce<ND, CAP>, a.n_vec);
+  static int occ_cache[kMaxDevices] = {};  // this instantiation's occupancy per device
+  int grid = occupancy_grid(k_reduce<ND, CAP>, a.n_vec, occ_cache);
   if (grid > kMaxPartialBlocks) grid = kMaxPartialBlocks;
   if (p.grid > 0 && p.grid < grid) grid = p.grid;
   k_reduce<ND, CAP><<<grid, kThreads, 0, s>>>(a);
@@ -586,17 +556,15 @@ cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s) {
   a.p16 = static_cast<uint16_t*>(p.param16);
   a.n_valid = p.n_valid;
   a.st = p.scratch;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  static bool attr_set[64] = {};
-  if (dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(k_update, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kUpdSmem);
+  int dev = 0;
+  const int sms = sm_count(&dev);
+  static bool attr_set[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_update, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kUpdSmem);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
   }
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long tiles = ((p.n_valid & ~7ll) + kUpdTile - 1) / kUpdTile;
   long long grid = tiles < sms ? tiles : sms;  // one CTA per SM, persistent
   if (grid < 1) grid = 1;

@@ -162,3 +162,8 @@ def test_scaler_and_state_calls_validate_before_touching_the_device():
         expect(z.ZERO_EINVAL, z.zero_plan_set_state, p, st)
         st.step = 3
         expect(z.ZERO_EUNBOUND, z.zero_plan_set_state, p, st)
+
+
+def test_selftest_rejects_bad_poll_counts():
+    for polls in (0, 2**24 + 1):
+        expect(z.ZERO_EINVAL, z.zero_selftest_wait, polls)

@@ -29,6 +29,7 @@ def run_gather(n, nd, align, offsets, dst_pad=0, src_pad=0, seed=0):
     dst = [d[dst_pad:] for d in dbase]
     plan = z.zero_plan_create(n, nd, 3, align, HP)
     z.zero_gather_layers(plan, offsets, shards, [d if d.numel() else None for d in dst])
+    assert z.zero_gather_status(plan) == 0
     torch.cuda.synchronize()
     host_shards = [h16(x) for x in shards]
     expected = oracle.gather(host_shards, s, offsets)
