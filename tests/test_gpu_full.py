@@ -30,22 +30,22 @@ def test_gpt2_small_flat_nd8_all_steps():
 
 def test_flat_1p3b_nd16_overflow_skip():
     w = wl.WORKLOADS["flat_1p3b_nd16_inf"]
-    r = Runner(w, mode="sampled", steps=4).run()
-    assert [x["skipped"] for x in r.results] == [0, 0, 1, 0]
-    assert [x["step"] for x in r.results] == [1, 2, 2, 3]
+    r = Runner(w, mode="sampled").run()  # all 8 steps
+    assert [x["skipped"] for x in r.results] == [0, 0, 1, 0, 0, 0, 0, 0]
+    assert [x["step"] for x in r.results] == [1, 2, 2, 3, 4, 5, 6, 7]
     assert r.exact
 
 
 def test_zero2_7b_rank0_nd8():
     w = wl.WORKLOADS["zero2_7b_rank0_nd8"]
-    r = Runner(w, mode="sampled", steps=2).run()
+    r = Runner(w, mode="sampled").run()  # all 5 steps
     assert all(x["skipped"] == 0 for x in r.results)
     assert r.exact
 
 
 def test_zero3_13b_rank0_nd64_step_and_gather():
     w = wl.WORKLOADS["zero3_13b_rank0_nd64"]
-    r = Runner(w, mode="sampled", steps=2).run()
+    r = Runner(w, mode="sampled").run()  # all 5 steps
     assert r.exact
     master, m, v, p16, ws = r.state
     del master, m, v, ws
