@@ -35,7 +35,7 @@ def test_tiny_zero2_workload_all_steps_bit_exact():
 
 
 @pytest.mark.parametrize("n", [1, 7, 8, 9, 1023, 4099, 70001])
-@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 8, 16, 17, 32, 64, 100])
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 8, 16, 17, 32, 64, 100, 256])
 def test_odd_shapes_and_rank_counts(n, nd):
     if n * nd > 2_000_000:
         n = 2_000_000 // nd
@@ -240,3 +240,40 @@ def test_dist_step_in_one_process_group_equals_step():
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
     finally:
         dist.destroy_process_group()
+
+
+def test_step_captured_in_a_cuda_graph_matches_eager_steps():
+    # the step's two launches make no host-side decision, so they can be captured once and
+    # replayed; replays must give the same bits as eager calls (including an overflow skip)
+    w = small(n=300_001, nd=8, r1=8, cfg=250, steps=4, inject=((2, 3, wl.POS_INF, 4321),))
+    first, n_span, n_valid = w.span()
+    results = []
+    for graph in (False, True):
+        master, m, v, p16, ws = wl.make_state(w)
+        plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+        z.zero_plan_bind(plan, 0, 8, master, m, v, p16, ws, 0)
+        grads = [torch.empty(n_span, dtype=torch.float16, device="cuda") for _ in range(8)]
+        infos = []
+        if graph:
+            wl.fill_grads(w, 0, grads)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                z.zero_shard_step(plan, 0, 8, grads, w.loss_scale, w.clip)
+            # capture does not run the kernels; replay each step after refilling the inputs
+            for step in range(w.steps):
+                wl.fill_grads(w, step, grads)
+                g.replay()
+                torch.cuda.synchronize()
+                infos.append(z.zero_step_result(plan).as_dict())
+        else:
+            for step in range(w.steps):
+                wl.fill_grads(w, step, grads)
+                z.zero_shard_step(plan, 0, 8, grads, w.loss_scale, w.clip)
+                infos.append(z.zero_step_result(plan).as_dict())
+        results.append((infos, [f32(master), f32(m), f32(v), h16(p16)]))
+        plan.close()
+    assert results[0][0] == results[1][0]
+    assert [x["skipped"] for x in results[0][0]] == [0, 0, 1, 0]
+    for a, b in zip(results[0][1], results[1][1]):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
