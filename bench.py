@@ -468,6 +468,10 @@ def run_gather(args, w):
     shards = wl.make_shards(w, shard0)
     wl.fill(shard0, wl.key(w, wl.SHARD16, 0, 0), w.shard_sigma, start=0, n_valid=w.n)
     offs = list(w.layers)
+    if args.layer_shift:
+        # move every interior layer boundary by a few elements: layers then start at
+        # addresses misaligned (mod 16 bytes) relative to the shards they copy from
+        offs = [offs[0]] + [o + args.layer_shift for o in offs[1:-1]] + [offs[-1]]
     dst = [torch.empty(offs[l + 1] - offs[l], dtype=torch.float16, device="cuda")
            for l in range(len(offs) - 1)]
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
@@ -503,6 +507,7 @@ def run_gather(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
         "vs_baseline": None, "dtype": "f16 (copy)", "data": "synthetic",
         "config": {"workload": w.name, "op": "gather", "n_params": w.n, "nd": w.nd,
+                   "layer_shift": args.layer_shift,
                    "layers": len(offs) - 1, "shard_len": s,
                    "l2": f"inputs larger than L2 ({2 * w.n / 1e9:.1f} GB of shards); no flush"},
         "e2e": None, "gpu_launches": int(kl[z.PROF_GATHER]),
@@ -533,6 +538,8 @@ def main(argv=None):
     ap.add_argument("--state", default="device", choices=["device", "host"],
                     help="where master/m/v/param16 live: HBM, or pinned Grace memory read "
                          "and written over NVLink-C2C")
+    ap.add_argument("--layer-shift", type=int, default=0,
+                    help="gather: shift interior layer boundaries by this many elements")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step from a CUDA graph (one per gradient set)")
     ap.add_argument("--one-set", action="store_true",

@@ -139,8 +139,9 @@ int64_t zero_workspace_bytes(const zero_plan* plan, int32_t r0, int32_t r1);
  *   param16: fp16[n], device, written by the step (the fp16 parameter copy);
  *   workspace: zero_workspace_bytes(plan, r0, r1) bytes of device memory, scratch;
  *   initial_step: the optimizer step counter t before the first step (>= 0).
- * Every pointer must be non-NULL and 16-byte aligned (ZERO_EALIGN otherwise). Elements
- * in the padding are never read or written. The first bind allocates the plan's device
+ * Every pointer must be non-NULL and 16-byte aligned (ZERO_EALIGN otherwise). The
+ * padding elements of master, exp_avg, exp_avg_sq and param16 are never read or written
+ * (gradient contributions there are read and ignored). The first bind allocates the plan's device
  * scratch on the current device; rebinding replaces the state pointers and resets the
  * step counter. Synchronous. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
 int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float* exp_avg,
@@ -160,7 +161,10 @@ int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float
  * exp_avg and exp_avg_sq with the fp16 cast into param16; the step counter advances
  * only on an applied step. Enqueued on stream; no host synchronisation. The two kernel
  * launches it makes contain no host-side decision, so the call can be captured in a
- * CUDA graph. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EUNBOUND, ZERO_ECUDA. */
+ * CUDA graph and replayed (the graph keeps the pointers it was captured with); make one
+ * ordinary call on the device first, so that the kernels' one-time per-device set-up
+ * happens outside the capture. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EUNBOUND,
+ * ZERO_ECUDA. */
 int zero_shard_step(zero_plan* plan, int32_t r0, int32_t r1, const void* const* grad_ptrs,
                     float loss_scale, float clip, void* stream);
 

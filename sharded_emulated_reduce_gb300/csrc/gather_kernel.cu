@@ -9,8 +9,9 @@
 // through a 4-stage ring of 32 KiB shared-memory buffers with TMA bulk copies: a bulk load
 // into a free buffer, then a bulk store out of it once the load has landed, several in
 // flight at once. The few elements before the first 16-byte-aligned destination address
-// and after the last are copied by the other threads, and a tile whose source and
-// destination are misaligned relative to each other is copied element by element.
+// and after the last are copied by the other threads. A tile whose source and destination
+// are misaligned relative to each other is copied by all threads with 16-byte loads that
+// are recombined in registers (funnel shifts) into aligned 16-byte stores.
 #include "bulk_async.h"
 #include "internal.h"
 
@@ -64,6 +65,62 @@ __device__ bool ring_copy(Ring& r, const unsigned char* src, unsigned char* dst,
   return true;
 }
 
+// Bytes [d, d+16) of the 32-byte concatenation lo|hi, for an even d in 2..14 (little
+// endian: lo.x holds bytes 0..3).
+__device__ __forceinline__ uint4 realign(const uint4& lo, const uint4& hi, int d) {
+  switch (d) {
+    case 2: return make_uint4(__funnelshift_r(lo.x, lo.y, 16), __funnelshift_r(lo.y, lo.z, 16),
+                              __funnelshift_r(lo.z, lo.w, 16), __funnelshift_r(lo.w, hi.x, 16));
+    case 4: return make_uint4(lo.y, lo.z, lo.w, hi.x);
+    case 6: return make_uint4(__funnelshift_r(lo.y, lo.z, 16), __funnelshift_r(lo.z, lo.w, 16),
+                              __funnelshift_r(lo.w, hi.x, 16), __funnelshift_r(hi.x, hi.y, 16));
+    case 8: return make_uint4(lo.z, lo.w, hi.x, hi.y);
+    case 10: return make_uint4(__funnelshift_r(lo.z, lo.w, 16), __funnelshift_r(lo.w, hi.x, 16),
+                               __funnelshift_r(hi.x, hi.y, 16), __funnelshift_r(hi.y, hi.z, 16));
+    case 12: return make_uint4(lo.w, hi.x, hi.y, hi.z);
+    default: return make_uint4(__funnelshift_r(lo.w, hi.x, 16), __funnelshift_r(hi.x, hi.y, 16),
+                               __funnelshift_r(hi.y, hi.z, 16), __funnelshift_r(hi.z, hi.w, 16));
+  }
+}
+
+// A tile whose source and destination differ in alignment modulo 16 bytes (all threads).
+// Destination vector j (16-byte aligned) is bytes [d, d+16) of the two aligned source
+// vectors W_j, W_{j+1} around it; a vector is used only when both lie inside the tile's
+// source range, and the remaining edge elements are copied one by one.
+__device__ void copy_realigned(const uint16_t* src, uint16_t* dst, long long n, long long head) {
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
+  const uintptr_t s_body = s0 + 2 * head;              // source of the first aligned dst vector
+  const int d = (int)(s_body & 15u);                   // 2..14
+  const uintptr_t a = s_body - d;                      // aligned source base
+  const uintptr_t s_end = s0 + 2 * n;
+  const long long nvec = (n - head) >> 3;              // dst vectors in the tile
+  const long long j_lo = a >= s0 ? 0 : 1;
+  long long j_hi = s_end >= a + 16 ? (long long)((s_end - a - 16) >> 4) : 0;
+  if (j_hi > nvec) j_hi = nvec;
+  if (j_hi < j_lo) j_hi = j_lo;                        // no vector fits
+  const uint4* w = reinterpret_cast<const uint4*>(a);
+  uint4* out = reinterpret_cast<uint4*>(dst + head);
+  // 8 destination vectors per thread per round: 16 loads in flight (W_{j+1} of one thread
+  // is W_j of the next, so half of them are served by L1), then 8 aligned stores
+  long long j = j_lo + threadIdx.x;
+  for (; j + 7 * kGatThreads < j_hi; j += 8 * kGatThreads) {
+    uint4 lo[8], hi[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      lo[u] = w[j + u * kGatThreads];
+      hi[u] = w[j + u * kGatThreads + 1];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) out[j + u * kGatThreads] = realign(lo[u], hi[u], d);
+  }
+  for (; j < j_hi; j += kGatThreads) out[j] = realign(w[j], w[j + 1], d);
+  long long v0 = head + 8 * j_lo, v1 = head + 8 * j_hi;  // vectors cover [v0, v1)
+  if (v0 > n) v0 = n;
+  if (v1 > n) v1 = n;
+  for (long long i = threadIdx.x; i < v0; i += kGatThreads) dst[i] = src[i];
+  for (long long i = v1 + threadIdx.x; i < n; i += kGatThreads) dst[i] = src[i];
+}
+
 // A CTA visits its tiles in increasing order, so the segment that holds a tile is found
 // by advancing a running index through the table.
 __global__ void __launch_bounds__(kGatThreads, 1) k_gather(const __grid_constant__ GatherLaunch a) {
@@ -90,7 +147,7 @@ __global__ void __launch_bounds__(kGatThreads, 1) k_gather(const __grid_constant
     long long head = (long long)(((16u - (unsigned)(da & 15u)) & 15u) >> 1);
     if (head > n) head = n;
     if (((sa + 2 * head) & 15u) != 0) {  // misaligned relative to each other
-      for (long long j = tid; j < n; j += kGatThreads) dst[j] = src[j];
+      copy_realigned(src, dst, n, head);
       continue;
     }
     const long long body = ((n - head) >> 3) << 3;  // elements moved by bulk copies

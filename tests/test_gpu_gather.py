@@ -54,6 +54,16 @@ def test_gather_matches_oracle(n, nd, offsets, dst_pad, src_pad):
     run_gather(n, nd, 8, offsets, dst_pad, src_pad)
 
 
+@pytest.mark.parametrize("rel", range(1, 8))
+def test_relatively_misaligned_source_and_destination(rel):
+    # destination buffers start `rel` elements off the source's alignment: every 2-byte
+    # relative offset modulo 16 bytes goes through the realigning vector path, over many
+    # 64 KiB tiles and their edges
+    run_gather(3_000_017, 8, 8, [0, 1_000_001, 1_000_003, 2_345_678, 3_000_017],
+               dst_pad=rel, src_pad=0, seed=rel)
+    run_gather(700_000, 4, 8, [0, 175_003, 700_000], dst_pad=0, src_pad=rel, seed=10 + rel)
+
+
 def test_stage2_full_buffer_gather():
     # ZeRO-1/2: one layer [0, N) reassembles the whole fp16 parameter buffer
     run_gather(124_439, 8, 128, [0, 124_439])

@@ -255,8 +255,14 @@ def test_step_captured_in_a_cuda_graph_matches_eager_steps():
         grads = [torch.empty(n_span, dtype=torch.float16, device="cuda") for _ in range(8)]
         infos = []
         if graph:
+            # one ordinary call on a throw-away plan does the per-device kernel set-up
+            warm = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+            wm, wmm, wv, wp, wws = wl.make_state(w)
+            z.zero_plan_bind(warm, 0, 8, wm, wmm, wv, wp, wws, 0)
             wl.fill_grads(w, 0, grads)
+            z.zero_shard_step(warm, 0, 8, grads, w.loss_scale, w.clip)
             torch.cuda.synchronize()
+            warm.close()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 z.zero_shard_step(plan, 0, 8, grads, w.loss_scale, w.clip)

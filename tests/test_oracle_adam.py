@@ -166,3 +166,26 @@ def test_param16_is_rounded_master():
     master, m, v, p16 = fresh_state(n, rng, 3.0)
     oracle.step(contrib, master, m, v, p16, 1.0, 0.0, oracle.Hyper(lr=0.1), 0)
     assert np.array_equal(p16, master.astype(np.float16).view(np.uint16))
+
+
+def test_decay_is_applied_before_the_adam_term():
+    # with lr * wd large, decaying after the Adam term instead of before moves the
+    # result by lr^2 * wd * u, far beyond rounding: torch's AdamW decays first
+    rng = np.random.default_rng(17)
+    n, ls = 4000, 1.0
+    hp = oracle.Hyper(lr=0.1, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.5)
+    master, m, v, p16 = fresh_state(n, rng, 1.0)
+    p = torch.nn.Parameter(torch.from_numpy(master.copy()))
+    opt = torch.optim.AdamW([p], lr=f32(hp.lr), betas=(f32(hp.beta1), f32(hp.beta2)),
+                            eps=f32(hp.eps), weight_decay=f32(hp.weight_decay), foreach=False)
+    t = 0
+    for _ in range(3):
+        contrib = [rand_f16(rng, n, 1.0) for _ in range(2)]
+        gsum = oracle.reduce(contrib)
+        sc = oracle.step(contrib, master, m, v, p16, ls, 0.0, hp, t)
+        t = sc.step
+        p.grad = torch.from_numpy(gsum * np.float32(sc.s))
+        opt.step()
+        assert np.allclose(master, p.detach().numpy(), rtol=1e-5, atol=1e-6)
+    # the other order would be off by about lr^2 * wd = 5e-3 per step
+    assert np.abs(master - p.detach().numpy()).max() < 1e-4
