@@ -70,3 +70,4 @@ def test_f32_to_f16_special_values():
     assert list(got[:4]) == [0x0000, 0x8000, 0x7C00, 0xFC00]
     assert (got[4] & 0x7C00) == 0x7C00 and (got[4] & 0x3FF) != 0
     assert list(got[5:]) == [0x3C00, 0xC000, 0x7BFF, 0x0001, 0x0000, 0x0001, 0x0400]
+
