@@ -208,7 +208,8 @@ int zero_step_result(zero_plan* plan, zero_step_info* out);
 int zero_gather_layers(zero_plan* plan, const int64_t* layer_offsets, int32_t n_layers,
                        const void* const* shard_ptrs, void* const* layer_dst, void* stream);
 
-/* Wait for the plan's last gather and report whether it finished: *status is 0, or 4 if a
+/* Wait for the plan's last gather and report whether it finished (the library's own
+ * failure reporting; the pages have no counterpart): *status is 0, or 4 if a
  * bulk copy did not arrive within its bounded wait and the gather stopped early (never
  * expected on a healthy GPU; the status is then cleared and ZERO_EDEVICE returned).
  * Errors: ZERO_EINVAL, ZERO_ECUDA, ZERO_EDEVICE. */
@@ -224,7 +225,8 @@ int zero_gather_status(zero_plan* plan, int32_t* status);
 int zero_memory_bytes(int64_t n_params, int32_t nd, int32_t align, int32_t stage,
                       int64_t* per_rank_bytes);
 
-/* Kernel timing with CUDA events on the launching stream, for profiling. When enabled,
+/* Kernel timing with CUDA events on the launching stream, for profiling (a measurement
+ * facility; the pages have no counterpart). When enabled,
  * every kernel the plan launches is bracketed by two events; zero_profile_read
  * synchronises and returns, per kernel kind (0 reduce, 1 update, 2 finalize, 3 gather),
  * the summed milliseconds and the launch count, then clears them if reset != 0. Off by
@@ -271,7 +273,8 @@ int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid, const void* 
  * ZERO_EINVAL, ZERO_EUNBOUND, ZERO_ECUDA. */
 int zero_plan_set_scaler(zero_plan* plan, const zero_loss_scaler* scaler);
 
-/* Device address of the current loss scale (one fp32 value in the plan's scratch). Valid
+/* Device address of the current loss scale (one fp32 value in the plan's scratch; part of
+ * the dynamic scaler above, which the pages do not describe). Valid
  * after zero_plan_bind and until zero_plan_destroy. Errors: ZERO_EINVAL, ZERO_EUNBOUND. */
 int zero_loss_scale_ptr(zero_plan* plan, float** dev_scale);
 
