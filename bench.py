@@ -15,8 +15,8 @@ logical ranks [g*Nd/N, (g+1)*Nd/N) of the same model (strong scaling); the one e
 step is an NCCL all-reduce of the 64-byte statistics buffer between the two halves of
 the step.
 
-``--impl reference`` times the CPU oracle (single-threaded C) on a bounded sample of the
-same workload instead; it needs no GPU.
+``--impl reference`` times the CPU oracle (its C steps partitioned over the host cores) on
+a bounded sample of the same workload instead; it needs no GPU.
 """
 from __future__ import annotations
 
@@ -130,43 +130,120 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------
 # CPU oracle timing (test infrastructure; the only place the bench runs the oracle)
 
-def cpu_sample(w, n):
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+GEN_CHUNK = 1 << 20  # elements per generator call (the counter-based streams split freely)
+
+
+def _generate(fn, n, pool):
+    import numpy as np
+    bounds = list(range(0, n, GEN_CHUNK)) + [n]
+    parts = list(pool.map(lambda i: fn(bounds[i], bounds[i + 1] - bounds[i]),
+                          range(len(bounds) - 1)))
+    return np.concatenate(parts) if len(parts) > 1 else parts[0]
+
+
+def cpu_sample(w, n, threads=None):
     """The first n parameters of the workload's span, generated on the CPU by the seeded
-    generator: two gradient sets and the initial master/m/v/param16."""
+    generator: two gradient sets and the initial master/m/v/param16. Every value depends
+    only on its index, so the arrays are generated in chunks on several threads."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import numpy as np
 
     import synth
     from synth import workloads as wl
     first = w.span()[0]
-    master = synth.values_f32(wl.key(w, synth.MASTER), w.master_sigma, first, n)
-    m = (synth.values_f32(wl.key(w, synth.EXP_AVG), w.m_sigma, first, n) if w.m_sigma > 0
-         else np.zeros(n, np.float32))
-    v = (synth.values_f32(wl.key(w, synth.EXP_AVG_SQ), w.v_sigma, first, n, absolute=True)
-         if w.v_sigma > 0 else np.zeros(n, np.float32))
-    p16 = master.astype(np.float16).view(np.uint16).copy()
-    grads = [[synth.values_f16(wl.key(w, synth.GRAD, st, k), w.grad_sigma * w.loss_scale,
-                               first, n) for k in range(w.nd)] for st in range(2)]
+    with ThreadPoolExecutor(threads or host_threads()) as pool:
+        def f32(kind, sigma, absolute=False):
+            return _generate(lambda a, k: synth.values_f32(wl.key(w, kind), sigma, first + a, k,
+                                                           absolute=absolute), n, pool)
+        master = f32(synth.MASTER, w.master_sigma)
+        m = f32(synth.EXP_AVG, w.m_sigma) if w.m_sigma > 0 else np.zeros(n, np.float32)
+        v = (f32(synth.EXP_AVG_SQ, w.v_sigma, absolute=True) if w.v_sigma > 0
+             else np.zeros(n, np.float32))
+        p16 = master.astype(np.float16).view(np.uint16).copy()
+        grads = [[_generate(lambda a, k, st=st, r=r: synth.values_f16(
+                      wl.key(w, synth.GRAD, st, r), w.grad_sigma * w.loss_scale, first + a, k),
+                      n, pool) for r in range(w.nd)] for st in range(2)]
     return grads, master, m, v, p16
 
 
-def oracle_steps(w, n, steps=None, seconds=None, warmup=0):
-    """Run the single-threaded oracle on a CPU sample of n parameters, either a fixed
-    number of steps or until ``seconds`` pass. Returns (params/s, steps, seconds)."""
+class PartitionedOracle:
+    """The oracle's shard step run on T host threads over disjoint slices of the span,
+    with the same results as one oracle.step over the whole span: each thread sums its
+    slice in rank order and takes its slice's non-finite count and exact integer sum of
+    squares; the counts and sums are added (exactly, as integers), the step's scalars are
+    computed once from the totals, and each thread then updates its own slice. ctypes
+    releases the interpreter lock during the oracle's C calls, so the slices run in
+    parallel."""
+
+    def __init__(self, n, threads):
+        from concurrent.futures import ThreadPoolExecutor
+        self.threads = max(1, min(threads, max(1, n // 64)))
+        cuts = [(n * i // self.threads) // 64 * 64 for i in range(self.threads)] + [n]
+        self.slices = [slice(cuts[i], cuts[i + 1]) for i in range(self.threads)]
+        self.pool = ThreadPoolExecutor(self.threads)
+
+    def step(self, grads, master, m, v, p16, loss_scale, clip, hp, t):
+        import oracle
+
+        def sums(sl):
+            gsum = oracle.reduce([c[sl] for c in grads])
+            bad, ss = oracle.stats(gsum)
+            return gsum, bad, ss
+
+        parts = list(self.pool.map(sums, self.slices))
+        sc = oracle.scalars(sum(p[1] for p in parts), sum(p[2] for p in parts), loss_scale,
+                            clip, hp, t)
+        list(self.pool.map(lambda i: oracle.adam(parts[i][0], master[self.slices[i]],
+                                                 m[self.slices[i]], v[self.slices[i]],
+                                                 p16[self.slices[i]], sc),
+                           range(self.threads)))
+        return sc
+
+    def close(self):
+        self.pool.shutdown()
+
+
+def oracle_steps(w, n, steps=None, seconds=None, warmup=0, threads=1, sample=None):
+    """Run the oracle on a CPU sample of n parameters (single-threaded, or partitioned over
+    ``threads`` host threads), either a fixed number of steps or until ``seconds`` pass.
+    Returns (params/s, steps, seconds, threads used)."""
     import oracle
-    grads, master, m, v, p16 = cpu_sample(w, n)
+    grads, master, m, v, p16 = sample if sample is not None else cpu_sample(w, n)
+    if sample is not None:  # the first n parameters of a larger sample
+        grads = [[c[:n] for c in g] for g in grads]
+        master, m, v, p16 = (x[:n].copy() for x in (master, m, v, p16))
     hp = oracle.Hyper(**w.hparams())
+    par = PartitionedOracle(n, threads) if threads > 1 else None
+
+    def one(g, t):
+        if par is not None:
+            return par.step(g, master, m, v, p16, w.loss_scale, w.clip, hp, t).step
+        return oracle.step(g, master, m, v, p16, w.loss_scale, w.clip, hp, t).step
+
     t = 0
     for i in range(warmup):
-        t = oracle.step(grads[i % 2], master, m, v, p16, w.loss_scale, w.clip, hp, t).step
+        t = one(grads[i % 2], t)
     done = 0
     t0 = time.perf_counter()
     while True:
-        t = oracle.step(grads[done % 2], master, m, v, p16, w.loss_scale, w.clip, hp, t).step
+        t = one(grads[done % 2], t)
         done += 1
         el = time.perf_counter() - t0
         if (steps is not None and done >= steps) or (seconds is not None and el >= seconds):
             break
-    return n * done / el, done, el
+    used = par.threads if par is not None else 1
+    if par is not None:
+        par.close()
+    return n * done / el, done, el, used
 
 
 def sample_size(w, max_params):
@@ -174,32 +251,103 @@ def sample_size(w, max_params):
     return max(8, n - n % 8)
 
 
-def oracle_sample_rate(w, seconds: float, max_params: int = 4_000_000):
-    n = sample_size(w, max_params)
-    rate, steps, el = oracle_steps(w, n, seconds=seconds)
-    desc = (f"oracle.step (single-threaded C, -O2) on the first {n:,} parameters of the "
-            f"span, {steps} steps in {el:.1f} s; norm and clip taken over the sample")
-    return rate, desc
+SAMPLE_PER_THREAD = 2_000_000  # parameters per host thread in the all-core sample
+SAMPLE_BYTES = 4e9             # host memory for the all-core sample at most
+
+
+def sample_bytes_per_param(w):
+    return 2 * 2 * w.nd + 4 * 4 + 2  # two gradient sets, master/m/v + the sum, param16
+
+
+def all_core_sample_size(w, threads):
+    n = min(threads * SAMPLE_PER_THREAD, int(SAMPLE_BYTES / sample_bytes_per_param(w)))
+    return sample_size(w, max(8, n))
+
+
+def oracle_sample_rate(w, seconds: float):
+    """The oracle on all host cores (partitioned) and on one core, each for about half of
+    ``seconds``, on one sample of the workload. Returns the cpu_baseline object."""
+    threads = host_threads()
+    n = all_core_sample_size(w, threads)
+    sample = cpu_sample(w, n, threads)
+    rate, steps, el, used = oracle_steps(w, n, seconds=seconds / 2, threads=threads,
+                                         sample=sample)
+    n1 = sample_size(w, min(n, 4_000_000))
+    rate1, steps1, el1, _ = oracle_steps(w, n1, seconds=seconds / 2, sample=sample)
+    return {
+        "value": rate, "unit": UNIT, "cores": used, "kind": "oracle",
+        "sample": (f"oracle reduce/stats/adam (C, -O2) partitioned over {used} host threads "
+                   f"with an exact integer combine of the statistics, on the first {n:,} "
+                   f"parameters of the span; {steps} steps in {el:.1f} s; norm and clip taken "
+                   f"over the sample"),
+        "single_thread": {"value": rate1, "cores": 1,
+                          "sample": f"oracle.step on the first {n1:,} parameters, {steps1} "
+                                    f"steps in {el1:.1f} s"},
+    }
+
+
+def gather_cpu_rate(w, seconds: float):
+    """The oracle's gather timed on the host cores on a scaled-down copy of the workload's
+    layout: nd shards of s' elements (s' chosen so the sample has about
+    SAMPLE_PER_THREAD parameters per thread) and the layer offsets scaled by s'/s; the
+    layers are split into contiguous groups, one oracle.gather call per group and thread.
+    Returns the cpu_baseline object (params/s)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    import synth
+    from synth import workloads as wl
+    threads = host_threads()
+    _, s = w.layout()
+    s_small = max(8, min(s, threads * SAMPLE_PER_THREAD // w.nd) // 8 * 8)
+    offs = [o * s_small // s for o in w.layers]
+    n_layers = len(offs) - 1
+    with ThreadPoolExecutor(threads) as pool:
+        shards = [_generate(lambda a, k, r=r: synth.values_f16(
+                      wl.key(w, synth.SHARD16, 0, r), w.shard_sigma, r * s_small + a, k),
+                      s_small, pool) for r in range(w.nd)]
+        groups = min(threads, n_layers)
+        cuts = [n_layers * i // groups for i in range(groups + 1)]
+        parts = [offs[cuts[i]:cuts[i + 1] + 1] for i in range(groups)]
+        done = 0
+        t0 = time.perf_counter()
+        while True:
+            list(pool.map(lambda o: oracle.gather(shards, s_small, o), parts))
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+    moved = offs[-1] - offs[0]
+    return {"value": moved * done / el, "unit": "params/s", "cores": groups, "kind": "oracle",
+            "sample": (f"oracle.gather (C) over {w.nd} shards of {s_small:,} elements into "
+                       f"{n_layers} layers ({moved:,} parameters; the workload's layer "
+                       f"offsets scaled by {s_small:,}/{s:,}), layer groups on {groups} host "
+                       f"threads; {done} passes in {el:.1f} s")}
 
 
 def run_reference(args, w):
     rank = env_int("RANK", 0)
     if rank != 0:
         return 0
-    # size one step's sample so that warmup + steps take about two minutes at most
-    rate0, _, _ = oracle_steps(w, sample_size(w, 65536), seconds=0.5)
+    # size the sample so that warmup + steps take about two minutes at most
+    threads = host_threads()
+    n_max = all_core_sample_size(w, threads)
+    probe = sample_size(w, min(n_max, threads * 65536))
+    rate0, _, _, _ = oracle_steps(w, probe, seconds=0.5, threads=threads)
     per_step = 120.0 / max(1, args.steps + args.warmup)
-    n = sample_size(w, int(max(8192, min(4_000_000, rate0 * per_step))))
-    value, _, el = oracle_steps(w, n, steps=args.steps, warmup=args.warmup)
-    sample = (f"oracle.step (single-threaded C) on the first {n:,} of {w.span()[2]:,} "
-              f"parameters per step; norm and clip over the sample")
+    n = sample_size(w, int(max(8192, min(n_max, rate0 * per_step))))
+    value, _, el, used = oracle_steps(w, n, steps=args.steps, warmup=args.warmup,
+                                      threads=threads)
+    sample = (f"oracle reduce/stats/adam (C) partitioned over {used} host threads, exact "
+              f"integer combine, on the first {n:,} of {w.span()[2]:,} parameters per step; "
+              f"norm and clip over the sample")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "strong",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_of(w, args.gpus),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -389,8 +537,7 @@ def run_ours(args, w0):
 
     if rank != 0:
         return 0
-    rate, desc = oracle_sample_rate(w0, args.cpu_seconds) if args.cpu_seconds > 0 \
-        else (None, "skipped")
+    cpu = oracle_sample_rate(w0, args.cpu_seconds) if args.cpu_seconds > 0 else None
     cfg = config_of(w0, world)
     if graphs is not None:
         cfg["launch"] = "CUDA graph replay (one graph per gradient set)"
@@ -410,8 +557,7 @@ def run_ours(args, w0):
                      "alg_frac": step_gbs / peak,
                      "min_moved_bytes_per_param": 2 * w0.nd + 34, "min_moved_gbs": moved,
                      "min_moved_frac": moved / peak, "peak": peak, "peak_kind": peak_kind},
-        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": cpu,
         "clocks": clk,
         "last_step": {k: info[k] for k in ("step", "skipped", "global_norm", "clip_coef")},
     }
@@ -513,9 +659,13 @@ def run_gather(args, w):
         "e2e": None, "gpu_launches": int(kl[z.PROF_GATHER]),
         "roofline": {"bound": "hbm", "kernel": "gather", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": load_traffic("gather", w), "alg_bytes_per_launch": alg,
+                     # the stored capture is of aligned layer boundaries
+                     "traffic": None if args.layer_shift else load_traffic("gather", w),
+                     "alg_bytes_per_launch": alg,
                      "avg_launch_ms": avg},
-        "cpu_baseline": None, "clocks": clk,
+        "cpu_baseline": (gather_cpu_rate(w, args.cpu_seconds) if args.cpu_seconds > 0
+                         else None),
+        "clocks": clk,
     }
     print(json.dumps(line))
     plan.close()

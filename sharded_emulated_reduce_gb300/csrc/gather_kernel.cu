@@ -9,9 +9,11 @@
 // through a 4-stage ring of 32 KiB shared-memory buffers with TMA bulk copies: a bulk load
 // into a free buffer, then a bulk store out of it once the load has landed, several in
 // flight at once. The few elements before the first 16-byte-aligned destination address
-// and after the last are copied by the other threads. A tile whose source and destination
-// are misaligned relative to each other is copied by all threads with 16-byte loads that
-// are recombined in registers (funnel shifts) into aligned 16-byte stores.
+// and after the last are copied by the other threads. Segments whose source and
+// destination are misaligned relative to each other go to a second kernel (the host sorts
+// them into their own table): bulk loads bring the aligned 16-byte source blocks around
+// each stretch of the tile into a shared-memory ring, and all threads recombine pairs of
+// blocks (funnel shifts) into aligned 16-byte stores to global memory.
 #include "bulk_async.h"
 #include "internal.h"
 
@@ -65,60 +67,74 @@ __device__ bool ring_copy(Ring& r, const unsigned char* src, unsigned char* dst,
   return true;
 }
 
-// Bytes [d, d+16) of the 32-byte concatenation lo|hi, for an even d in 2..14 (little
+// Bytes [D, D+16) of the 32-byte concatenation lo|hi, for an even D in 0..14 (little
 // endian: lo.x holds bytes 0..3).
-__device__ __forceinline__ uint4 realign(const uint4& lo, const uint4& hi, int d) {
-  switch (d) {
-    case 2: return make_uint4(__funnelshift_r(lo.x, lo.y, 16), __funnelshift_r(lo.y, lo.z, 16),
-                              __funnelshift_r(lo.z, lo.w, 16), __funnelshift_r(lo.w, hi.x, 16));
-    case 4: return make_uint4(lo.y, lo.z, lo.w, hi.x);
-    case 6: return make_uint4(__funnelshift_r(lo.y, lo.z, 16), __funnelshift_r(lo.z, lo.w, 16),
-                              __funnelshift_r(lo.w, hi.x, 16), __funnelshift_r(hi.x, hi.y, 16));
-    case 8: return make_uint4(lo.z, lo.w, hi.x, hi.y);
-    case 10: return make_uint4(__funnelshift_r(lo.z, lo.w, 16), __funnelshift_r(lo.w, hi.x, 16),
-                               __funnelshift_r(hi.x, hi.y, 16), __funnelshift_r(hi.y, hi.z, 16));
-    case 12: return make_uint4(lo.w, hi.x, hi.y, hi.z);
-    default: return make_uint4(__funnelshift_r(lo.w, hi.x, 16), __funnelshift_r(hi.x, hi.y, 16),
-                               __funnelshift_r(hi.y, hi.z, 16), __funnelshift_r(hi.z, hi.w, 16));
+template <int D>
+__device__ __forceinline__ uint4 realign(const uint4& lo, const uint4& hi) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  constexpr int q = D / 4;  // first word
+  if constexpr (D % 4 == 0) {
+    return make_uint4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+  } else {
+    return make_uint4(__funnelshift_r(w[q], w[q + 1], 16), __funnelshift_r(w[q + 1], w[q + 2], 16),
+                      __funnelshift_r(w[q + 2], w[q + 3], 16), __funnelshift_r(w[q + 3], w[q + 4], 16));
   }
 }
 
-// A tile whose source and destination differ in alignment modulo 16 bytes (all threads).
-// Destination vector j (16-byte aligned) is bytes [d, d+16) of the two aligned source
-// vectors W_j, W_{j+1} around it; a vector is used only when both lie inside the tile's
-// source range, and the remaining edge elements are copied one by one.
-__device__ void copy_realigned(const uint16_t* src, uint16_t* dst, long long n, long long head) {
-  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
-  const uintptr_t s_body = s0 + 2 * head;              // source of the first aligned dst vector
-  const int d = (int)(s_body & 15u);                   // 2..14
-  const uintptr_t a = s_body - d;                      // aligned source base
-  const uintptr_t s_end = s0 + 2 * n;
-  const long long nvec = (n - head) >> 3;              // dst vectors in the tile
-  const long long j_lo = a >= s0 ? 0 : 1;
-  long long j_hi = s_end >= a + 16 ? (long long)((s_end - a - 16) >> 4) : 0;
-  if (j_hi > nvec) j_hi = nvec;
-  if (j_hi < j_lo) j_hi = j_lo;                        // no vector fits
-  const uint4* w = reinterpret_cast<const uint4*>(a);
-  uint4* out = reinterpret_cast<uint4*>(dst + head);
-  // 8 destination vectors per thread per round: 16 loads in flight (W_{j+1} of one thread
-  // is W_j of the next, so half of them are served by L1), then 8 aligned stores
-  long long j = j_lo + threadIdx.x;
-  for (; j + 7 * kGatThreads < j_hi; j += 8 * kGatThreads) {
-    uint4 lo[8], hi[8];
+// One stretch of nv destination vectors from the nv + 1 source blocks in shared memory
+// (all threads; D fixed per tile, so the loop has no branch on it).
+template <int D, int NT>
+__device__ __forceinline__ void realign_stretch(const uint4* w, uint4* out, long long nv) {
+  long long i = threadIdx.x;
+  for (; i + 7 * NT < nv; i += 8 * NT) {
+    uint4 r[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      lo[u] = w[j + u * kGatThreads];
-      hi[u] = w[j + u * kGatThreads + 1];
-    }
+    for (int u = 0; u < 8; ++u) r[u] = realign<D>(w[i + u * NT], w[i + u * NT + 1]);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) out[j + u * kGatThreads] = realign(lo[u], hi[u], d);
+    for (int u = 0; u < 8; ++u) out[i + u * NT] = r[u];
   }
-  for (; j < j_hi; j += kGatThreads) out[j] = realign(w[j], w[j + 1], d);
-  long long v0 = head + 8 * j_lo, v1 = head + 8 * j_hi;  // vectors cover [v0, v1)
-  if (v0 > n) v0 = n;
-  if (v1 > n) v1 = n;
-  for (long long i = threadIdx.x; i < v0; i += kGatThreads) dst[i] = src[i];
-  for (long long i = v1 + threadIdx.x; i < n; i += kGatThreads) dst[i] = src[i];
+  for (; i < nv; i += NT) out[i] = realign<D>(w[i], w[i + 1]);
+}
+
+// Geometry of a tile whose source and destination differ in alignment modulo 16 bytes.
+// Destination vector j (16-byte aligned, at dst + head + 8j) is bytes [d, d+16) of the two
+// aligned source blocks W_j, W_{j+1} (16 bytes each, from a); vector j is used only for
+// j_lo <= j < j_hi, where both blocks lie inside the tile's source range, and the elements
+// outside [v0, v1) are copied one by one.
+struct MisTile {
+  const uint16_t* src;
+  uint16_t* dst;
+  long long n, head, j_lo, j_hi, v0, v1;
+  uintptr_t a;
+  int d;  // 2..14
+};
+
+__device__ __forceinline__ MisTile mis_tile(const GatherLaunch& L, int& seg, long long t) {
+  while (seg + 1 < L.nseg && L.seg[seg + 1].tile_begin <= t) ++seg;
+  const GatherSeg& sg = L.seg[seg];
+  const long long e0 = (t - sg.tile_begin) * kGatherTile;
+  MisTile m;
+  m.n = sg.len - e0;
+  if (m.n > kGatherTile) m.n = kGatherTile;
+  m.src = sg.src + e0;
+  m.dst = sg.dst + e0;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(m.src);
+  m.head = (long long)(((16u - (unsigned)(reinterpret_cast<uintptr_t>(m.dst) & 15u)) & 15u) >> 1);
+  if (m.head > m.n) m.head = m.n;
+  const uintptr_t s_body = s0 + 2 * m.head;  // source of the first aligned dst vector
+  m.d = (int)(s_body & 15u);
+  m.a = s_body - m.d;
+  const uintptr_t s_end = s0 + 2 * m.n;
+  const long long nvec = (m.n - m.head) >> 3;
+  m.j_lo = m.a >= s0 ? 0 : 1;
+  m.j_hi = s_end >= m.a + 16 ? (long long)((s_end - m.a - 16) >> 4) : 0;
+  if (m.j_hi > nvec) m.j_hi = nvec;
+  if (m.j_hi < m.j_lo) m.j_hi = m.j_lo;  // no vector fits
+  m.v0 = m.head + 8 * m.j_lo;
+  m.v1 = m.head + 8 * m.j_hi;
+  if (m.v0 > m.n) m.v0 = m.n;
+  if (m.v1 > m.n) m.v1 = m.n;
+  return m;
 }
 
 // A CTA visits its tiles in increasing order, so the segment that holds a tile is found
@@ -146,8 +162,8 @@ __global__ void __launch_bounds__(kGatThreads, 1) k_gather(const __grid_constant
     const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
     long long head = (long long)(((16u - (unsigned)(da & 15u)) & 15u) >> 1);
     if (head > n) head = n;
-    if (((sa + 2 * head) & 15u) != 0) {  // misaligned relative to each other
-      copy_realigned(src, dst, n, head);
+    if (((sa + 2 * head) & 15u) != 0) {  // misaligned relative to each other: the host
+      for (long long i = tid; i < n; i += kGatThreads) dst[i] = src[i];  // sends none here
       continue;
     }
     const long long body = ((n - head) >> 3) << 3;  // elements moved by bulk copies
@@ -162,6 +178,107 @@ __global__ void __launch_bounds__(kGatThreads, 1) k_gather(const __grid_constant
   if (tid == 0) {
     bulk_wait_all();
     if (!ok && a.status) atomicExch(a.status, kStatusGatherWait);
+  }
+}
+
+// Segments whose source and destination differ in alignment modulo 16 bytes. A tile's
+// vectors are cut into stretches of up to kMisVecs; thread 0 bulk-loads the kMisVecs + 1
+// source blocks of a stretch into a ring stage (kMisStages stages, up to two tiles ahead),
+// and after the stage has landed every thread builds its destination vectors from pairs of
+// adjacent blocks and stores them. The stage is refilled once all threads are past it.
+constexpr int kMisThreads = 256;
+constexpr int kMisStages = 4;
+constexpr long long kMisVecs = 2048;              // destination vectors per stretch
+constexpr uint32_t kMisStageBytes = 32768 + 128;  // (kMisVecs + 1) blocks, rounded to 128 B
+constexpr size_t kMisSmem = (size_t)kMisStages * kMisStageBytes + kMisStages * sizeof(uint64_t);
+
+// Walks this CTA's tiles and their non-empty stretches in the order they are consumed.
+struct StretchIt {
+  long long t;
+  long long h;  // next stretch of tile t
+  int seg;
+};
+
+// Next stretch: source blocks [a + 16 jb, + bytes) for destination vectors jb.. of its tile.
+__device__ __forceinline__ bool next_stretch(const GatherLaunch& L, StretchIt& it,
+                                             const unsigned char** src, uint32_t* bytes) {
+  while (it.t < L.tiles) {
+    const MisTile m = mis_tile(L, it.seg, it.t);
+    const long long jb = m.j_lo + it.h * kMisVecs;
+    if (jb < m.j_hi) {
+      long long nv = m.j_hi - jb;
+      if (nv > kMisVecs) nv = kMisVecs;
+      *src = reinterpret_cast<const unsigned char*>(m.a) + 16 * jb;
+      *bytes = (uint32_t)(16 * (nv + 1));
+      ++it.h;
+      return true;
+    }
+    it.t += gridDim.x;
+    it.h = 0;
+  }
+  return false;
+}
+
+__global__ void __launch_bounds__(kMisThreads, 1)
+    k_gather_realign(const __grid_constant__ GatherLaunch L) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kMisStages * kMisStageBytes);
+  const int tid = threadIdx.x;
+  StretchIt prod{(long long)blockIdx.x, 0, 0};  // thread 0's issue position
+  long long issued = 0;                         // stretches issued (thread 0)
+  auto issue = [&]() {
+    const unsigned char* src;
+    uint32_t bytes;
+    if (!next_stretch(L, prod, &src, &bytes)) return;
+    const int s = (int)(issued % kMisStages);
+    mbar_expect_tx(&full[s], bytes);
+    bulk_load(smem + (size_t)s * kMisStageBytes, src, bytes, &full[s]);
+    ++issued;
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kMisStages; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
+    for (int s = 0; s < kMisStages; ++s) issue();
+  }
+  __syncthreads();
+  long long q = 0;  // stretches consumed
+  int seg = 0;
+  bool ok = true;
+  for (long long t = blockIdx.x; t < L.tiles && ok; t += gridDim.x) {
+    const MisTile m = mis_tile(L, seg, t);
+    for (long long i = tid; i < m.v0; i += kMisThreads) m.dst[i] = m.src[i];
+    for (long long i = m.v1 + tid; i < m.n; i += kMisThreads) m.dst[i] = m.src[i];
+    uint4* out = reinterpret_cast<uint4*>(m.dst + m.head);
+    for (long long jb = m.j_lo; jb < m.j_hi && ok; jb += kMisVecs) {
+      long long nv = m.j_hi - jb;
+      if (nv > kMisVecs) nv = kMisVecs;
+      const int s = (int)(q % kMisStages);
+      bool landed = mbar_wait(&full[s], (uint32_t)((q / kMisStages) & 1));
+      if (landed) {
+        const uint4* w = reinterpret_cast<const uint4*>(smem + (size_t)s * kMisStageBytes);
+        switch (m.d) {  // even byte offsets 2..14 (0 only in tiles without vectors)
+          case 0: realign_stretch<0, kMisThreads>(w, out + jb, nv); break;
+          case 2: realign_stretch<2, kMisThreads>(w, out + jb, nv); break;
+          case 4: realign_stretch<4, kMisThreads>(w, out + jb, nv); break;
+          case 6: realign_stretch<6, kMisThreads>(w, out + jb, nv); break;
+          case 8: realign_stretch<8, kMisThreads>(w, out + jb, nv); break;
+          case 10: realign_stretch<10, kMisThreads>(w, out + jb, nv); break;
+          case 12: realign_stretch<12, kMisThreads>(w, out + jb, nv); break;
+          default: realign_stretch<14, kMisThreads>(w, out + jb, nv); break;
+        }
+      }
+      ok = __syncthreads_and(landed);  // every thread is done with stage s
+      if (ok) {
+        ++q;
+        if (tid == 0) issue();  // into stage s, the one just freed
+      }
+    }
+  }
+  if (tid == 0) {
+    // a wait that gave up: let every load still in flight land before the CTA exits
+    for (long long k = q; k < issued; ++k)
+      mbar_wait(&full[(int)(k % kMisStages)], (uint32_t)((k / kMisStages) & 1));
+    if (!ok && L.status) atomicExch(L.status, kStatusGatherWait);
   }
 }
 
@@ -193,6 +310,18 @@ cudaError_t launch_gather(const GatherLaunch& p, cudaStream_t s) {
     e = cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
+  }
+  if (p.realign) {
+    static bool mis_attr_set[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices || !mis_attr_set[dev]) {
+      e = cudaFuncSetAttribute(k_gather_realign, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kMisSmem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < kMaxDevices) mis_attr_set[dev] = true;
+    }
+    const int grid = p.grid > 0 ? p.grid : gather_grid(p.tiles);
+    k_gather_realign<<<grid, kMisThreads, kMisSmem, s>>>(p);
+    return cudaGetLastError();
   }
   const int grid = p.grid > 0 ? p.grid : gather_grid(p.tiles);
   k_gather<<<grid, kGatThreads, kGatSmem, s>>>(p);

@@ -88,6 +88,8 @@ struct GatherLaunch {
   int64_t tiles;       // total tiles over all segments
   int grid;
   int32_t* status;     // set to kStatusGatherWait if a bounded wait expires
+  int realign;         // 1: every segment's source and destination differ in alignment
+                       // modulo 16 bytes (k_gather_realign); 0: they agree (k_gather)
 };
 
 constexpr int64_t kGatherTile = 32768;  // elements per gather tile (64 KiB)

@@ -458,14 +458,18 @@ int zero_gather_layers(zero_plan* p, const int64_t* offs, int32_t n_layers,
   int rc0 = ensure_scratch(p, dev);  // holds the gather's status word
   if (rc0) return rc0;
 
-  // Cut each layer at shard boundaries; number the tiles of all segments in order.
+  // Cut each layer at shard boundaries; a segment goes to the table of its alignment class
+  // (source and destination equal modulo 16 bytes, or not); tiles are numbered in order.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  zero::GatherLaunch gl;
-  gl.nseg = 0;
-  gl.tiles = 0;
-  gl.grid = 0;
-  gl.status = &p->scratch->gather_status;
-  auto flush = [&]() -> int {
+  zero::GatherLaunch tables[2];
+  for (int k = 0; k < 2; ++k) {
+    tables[k].nseg = 0;
+    tables[k].tiles = 0;
+    tables[k].grid = 0;
+    tables[k].status = &p->scratch->gather_status;
+    tables[k].realign = k;
+  }
+  auto flush = [&](zero::GatherLaunch& gl) -> int {
     if (gl.nseg == 0) return ZERO_OK;
     EventPair ev;
     prof_begin(p, s, &ev);
@@ -482,19 +486,24 @@ int zero_gather_layers(zero_plan* p, const int64_t* offs, int32_t n_layers,
     for (int64_t r = a / p->s; r * p->s < b; ++r) {
       const int64_t lo = std::max(a, r * p->s), hi = std::min(b, (r + 1) * p->s);
       if (hi <= lo) continue;
+      const uint16_t* src = static_cast<const uint16_t*>(shards[r]) + (lo - r * p->s);
+      uint16_t* dptr = static_cast<uint16_t*>(dst[l]) + (lo - a);
+      const int k = ((reinterpret_cast<uintptr_t>(src) - reinterpret_cast<uintptr_t>(dptr)) & 15u) ? 1 : 0;
+      zero::GatherLaunch& gl = tables[k];
       if (gl.nseg == zero::kGatherSegs) {
-        int rc = flush();
+        int rc = flush(gl);
         if (rc) return rc;
       }
       zero::GatherSeg& sg = gl.seg[gl.nseg++];
-      sg.src = static_cast<const uint16_t*>(shards[r]) + (lo - r * p->s);
-      sg.dst = static_cast<uint16_t*>(dst[l]) + (lo - a);
+      sg.src = src;
+      sg.dst = dptr;
       sg.len = hi - lo;
       sg.tile_begin = gl.tiles;
       gl.tiles += (sg.len + zero::kGatherTile - 1) / zero::kGatherTile;
     }
   }
-  rc0 = flush();
+  rc0 = flush(tables[0]);
+  if (!rc0) rc0 = flush(tables[1]);
   if (!rc0) p->gather_stream = s;
   return rc0;
 }

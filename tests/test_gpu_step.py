@@ -283,3 +283,36 @@ def test_step_captured_in_a_cuda_graph_matches_eager_steps():
     assert [x["skipped"] for x in results[0][0]] == [0, 0, 1, 0]
     for a, b in zip(results[0][1], results[1][1]):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_two_plans_on_two_streams_concurrently():
+    # plans keep separate scratch, so two steps in flight at once on different streams
+    # give the same bits as each run alone
+    ws_ = [small(n=400_003, nd=4, cfg=260 + k, steps=3) for k in range(2)]
+    alone = []
+    for w in ws_:
+        r = Runner(w).run()
+        assert r.exact
+        alone.append([f32(t).copy() if t.dtype == torch.float32 else h16(t).copy()
+                      for t in r.state[:4]])
+        r.plan.close()
+    plans, states, grads = [], [], []
+    for w in ws_:
+        st = wl.make_state(w)
+        p = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+        z.zero_plan_bind(p, 0, w.nd, *st, 0)
+        plans.append(p)
+        states.append(st)
+        grads.append([[g for g in wl.make_grads(w, s)] for s in range(w.steps)])
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in range(3):
+        for k in range(2):
+            with torch.cuda.stream(streams[k]):
+                z.zero_shard_step(plans[k], 0, 4, grads[k][s], ws_[k].loss_scale, ws_[k].clip)
+    torch.cuda.synchronize()
+    for k in range(2):
+        got = [f32(t) if t.dtype == torch.float32 else h16(t) for t in states[k][:4]]
+        for a, b in zip(got, alone[k]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+        plans[k].close()
