@@ -38,10 +38,24 @@ struct DevPartial {
   long long pad;
 };
 
+// The step's scalars that depend only on the step counter t and the hyperparameters.
+// A CTA of the reduce kernel with no reduce work computes them for the next step (t + 1)
+// while the others reduce, so that the serial combine at the end of the next step's
+// reduce finds them ready; slot t & 1 holds those for t. The tag (t and the
+// hyperparameters) decides whether a slot may be used.
+struct DevPre {
+  float omb1, omb2, bc1, bc2, decay;
+  float lr, beta1, beta2, weight_decay;  // tag: the hyperparameters
+  int32_t valid;                         // kPreValid once written (zeroed scratch: not)
+  long long t;                           // tag: the step counter
+};
+constexpr int32_t kPreValid = 0x50524531;
+
 // The plan's device scratch (one allocation, < 64 KiB).
 struct DevScratch {
   long long stats[ZERO_STATS_WORDS];  // exchange buffer (see zero_shard_stats)
   DevScalars sc;
+  DevPre pre[2];
   DevScaler scaler;
   long long step;       // optimizer step counter t
   unsigned int ticket;    // arrival counter of the reduce CTAs

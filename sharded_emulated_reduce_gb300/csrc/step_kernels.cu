@@ -84,12 +84,62 @@ __device__ double u128_to_double(U128 a) {
   return ldexp(__ull2double_rn(top), shift);
 }
 
+// The scalars that depend only on t and the hyperparameters: double arithmetic, each
+// operation rounded to nearest, then one rounding to fp32. The two powers dominate the
+// cost (double precision is slow on this part).
+__device__ __forceinline__ DevPre pre_scalars(long long t, const HostHParams& hp) {
+  DevPre p;
+  const double tp = (double)(t + 1);
+  p.omb1 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta1));
+  p.omb2 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta2));
+  p.bc1 = __double2float_rn(__dadd_rn(1.0, -pow((double)hp.beta1, tp)));
+  p.bc2 = __double2float_rn(__dadd_rn(1.0, -pow((double)hp.beta2, tp)));
+  p.decay = __double2float_rn(__dadd_rn(1.0, -__dmul_rn((double)hp.lr, (double)hp.weight_decay)));
+  p.lr = hp.lr;
+  p.beta1 = hp.beta1;
+  p.beta2 = hp.beta2;
+  p.weight_decay = hp.weight_decay;
+  p.valid = kPreValid;
+  p.t = t;
+  return p;
+}
+
+// The same, as a call (kept out of line where it would crowd a hot kernel's registers).
+__device__ __noinline__ DevPre pre_scalars_call(long long t, const HostHParams& hp) {
+  return pre_scalars(t, hp);
+}
+
+// Whether slot `p` holds the t-only scalars of step counter t under hp (read through L2).
+__device__ __forceinline__ bool pre_matches(const DevPre* p, long long t, const HostHParams& hp) {
+  return __ldcg(&p->valid) == kPreValid && __ldcg(&p->t) == t && __ldcg(&p->lr) == hp.lr &&
+         __ldcg(&p->beta1) == hp.beta1 &&
+         __ldcg(&p->beta2) == hp.beta2 && __ldcg(&p->weight_decay) == hp.weight_decay;
+}
+
 // The step's scalars from its statistics (one thread). Double arithmetic, each
-// operation rounded to nearest, then one rounding to fp32.
+// operation rounded to nearest, then one rounding to fp32. With CACHED, the t-only
+// scalars come from slot t & 1 when its tag matches (else they are computed here);
+// without, they are computed here.
+template <bool CACHED>
 __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float loss_scale_arg,
                                 float clip, const HostHParams& hp) {
   DevScalars sc;
   const long long t = st->step;
+  DevPre pre;
+  if constexpr (CACHED) {
+    const DevPre* slot = &st->pre[t & 1];
+    if (pre_matches(slot, t, hp)) {
+      pre.omb1 = __ldcg(&slot->omb1);
+      pre.omb2 = __ldcg(&slot->omb2);
+      pre.bc1 = __ldcg(&slot->bc1);
+      pre.bc2 = __ldcg(&slot->bc2);
+      pre.decay = __ldcg(&slot->decay);
+    } else {
+      pre = pre_scalars_call(t, hp);
+    }
+  } else {
+    pre = pre_scalars(t, hp);
+  }
   // with the dynamic scaler on, the gradients carry the device-resident scale
   DevScaler scaler = st->scaler;
   const bool dynamic = scaler.interval > 0;
@@ -115,13 +165,12 @@ __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float lo
     sc.clip_coef = coef;
     sc.step = t + 1;
   }
-  const double tp = (double)(t + 1);
   sc.s = __double2float_rn(__ddiv_rn(sc.clip_coef, (double)loss_scale));
-  sc.omb1 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta1));
-  sc.omb2 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta2));
-  sc.bc1 = __double2float_rn(__dadd_rn(1.0, -pow((double)hp.beta1, tp)));
-  sc.bc2 = __double2float_rn(__dadd_rn(1.0, -pow((double)hp.beta2, tp)));
-  sc.decay = __double2float_rn(__dadd_rn(1.0, -__dmul_rn((double)hp.lr, (double)hp.weight_decay)));
+  sc.omb1 = pre.omb1;
+  sc.omb2 = pre.omb2;
+  sc.bc1 = pre.bc1;
+  sc.bc2 = pre.bc2;
+  sc.decay = pre.decay;
   sc.lr = hp.lr;
   sc.beta1 = hp.beta1;
   sc.beta2 = hp.beta2;
@@ -219,12 +268,29 @@ __device__ __forceinline__ void sum_group(const ReduceArgs<CAP>& a, long long v,
   }
 }
 
-template <int ND, int CAP>
+// With PRE, CTA 0 has no reduce work: it computes the t-only scalars of the next step
+// (counter t + 1) into slot (t + 1) & 1 unless that slot holds them already, and takes
+// no part in the combine, which then finds this step's in slot t & 1. The other CTAs
+// reduce; the last of them to finish combines their partials.
+template <int ND, int CAP, bool PRE>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ ReduceArgs<CAP> a) {
+  DevScratch* st = a.st;
+  if constexpr (PRE) {
+    if (blockIdx.x == 0) {
+      if (threadIdx.x == 0) {
+        const long long tn = st->step + 1;
+        DevPre* slot = &st->pre[tn & 1];
+        if (!pre_matches(slot, tn, a.hp)) *slot = pre_scalars_call(tn, a.hp);
+      }
+      return;
+    }
+  }
   U128 acc{0, 0};
   long long bad = 0;
-  const long long stride = (long long)gridDim.x * kThreads;
-  for (long long v = (long long)blockIdx.x * kThreads + threadIdx.x; v < a.n_vec; v += stride) {
+  const unsigned nred = gridDim.x - (PRE ? 1u : 0u);  // reducing CTAs
+  const unsigned b = blockIdx.x - (PRE ? 1u : 0u);
+  const long long stride = (long long)nred * kThreads;
+  for (long long v = (long long)b * kThreads + threadIdx.x; v < a.n_vec; v += stride) {
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     sum_group<ND, CAP>(a, v, s);
     const long long base = v * 8;
@@ -252,21 +318,20 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Red
   // CTA partial, then the last CTA to arrive combines all partials (no waiting).
   block_reduce<kThreads>(acc, bad);
   __shared__ int s_last;
-  DevScratch* st = a.st;
   if (threadIdx.x == 0) {
-    st->partials[blockIdx.x].lo = acc.lo;
-    st->partials[blockIdx.x].hi = acc.hi;
-    st->partials[blockIdx.x].bad = bad;
+    st->partials[b].lo = acc.lo;
+    st->partials[b].hi = acc.hi;
+    st->partials[b].bad = bad;
     __threadfence();
     const unsigned prev = atomicAdd(&st->ticket, 1u);
-    s_last = prev == gridDim.x - 1;
+    s_last = prev == nred - 1;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   U128 tot{0, 0};
   long long tb = 0;
-  for (int i = threadIdx.x; i < (int)gridDim.x; i += kThreads) {
+  for (int i = threadIdx.x; i < (int)nred; i += kThreads) {
     const DevPartial* p = &st->partials[i];
     add128(tot, __ldcg(&p->lo), __ldcg(&p->hi));
     tb += __ldcg(&p->bad);
@@ -279,7 +344,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Red
     st->stats[3] = (long long)(tot.hi & 0xffffffffull);
     st->stats[4] = (long long)(tot.hi >> 32);
     st->stats[5] = st->stats[6] = st->stats[7] = 0;
-    if (a.finalize) compute_scalars(st, tb, tot, a.loss_scale, a.clip, a.hp);
+    if (a.finalize) compute_scalars<PRE>(st, tb, tot, a.loss_scale, a.clip, a.hp);
     st->ticket = 0;
   }
 }
@@ -298,7 +363,7 @@ __global__ void k_finalize(DevScratch* st, float loss_scale, float clip, HostHPa
       default: add128(ss, 0ull, l << 32); break;
     }
   }
-  compute_scalars(st, bad, ss, loss_scale, clip, hp);
+  compute_scalars<true>(st, bad, ss, loss_scale, clip, hp);
 }
 
 struct UpdateArgs {
@@ -485,7 +550,8 @@ int sm_count(int* dev_out) {
 // needs. `per_sm` is the caller's per-device cache for this kernel (one static table per
 // launcher instantiation, because kernels of the same signature differ in occupancy).
 template <typename K>
-int occupancy_grid(K kernel, long long work_items, int (&per_sm)[kMaxDevices]) {
+int occupancy_grid(K kernel, long long work_items, int (&per_sm)[kMaxDevices],
+                   int* resident = nullptr) {
   int dev = 0;
   const int sms = sm_count(&dev);
   int occ = 0;
@@ -497,6 +563,7 @@ int occupancy_grid(K kernel, long long work_items, int (&per_sm)[kMaxDevices]) {
     if (dev >= 0 && dev < kMaxDevices) per_sm[dev] = occ;
   }
   long long g = (long long)sms * occ;
+  if (resident) *resident = (int)(g < 0x7fffffff ? g : 0x7fffffff);
   const long long need = (work_items + kThreads - 1) / kThreads;
   if (g > need) g = need;
   if (g < 1) g = 1;
@@ -517,10 +584,18 @@ cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s) {
   a.nd = p.nd;
   a.finalize = p.finalize ? 1 : 0;
   static int occ_cache[kMaxDevices] = {};  // this instantiation's occupancy per device
-  int grid = occupancy_grid(k_reduce<ND, CAP>, a.n_vec, occ_cache);
-  if (grid > kMaxPartialBlocks) grid = kMaxPartialBlocks;
+  // One wave of reducing CTAs. When the span needs less than a wave, a spare CTA slot
+  // computes the next step's t-only scalars, which takes their double-precision powers
+  // off the serial combine; a full wave keeps every slot for the reduce (one CTA fewer
+  // would cost more than the powers) and computes them in the combine.
+  int resident = 0;
+  int grid = occupancy_grid(k_reduce<ND, CAP, false>, a.n_vec, occ_cache, &resident);
   if (p.grid > 0 && p.grid < grid) grid = p.grid;
-  k_reduce<ND, CAP><<<grid, kThreads, 0, s>>>(a);
+  if (grid > kMaxPartialBlocks) grid = kMaxPartialBlocks;
+  if (grid < resident)
+    k_reduce<ND, CAP, true><<<grid + 1, kThreads, 0, s>>>(a);
+  else
+    k_reduce<ND, CAP, false><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

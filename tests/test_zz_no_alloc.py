@@ -67,6 +67,40 @@ def test_noalloc_skips_an_overflow_step_and_keeps_the_counter():
     assert not master.any() and not m.any() and not v.any()
 
 
+def test_noalloc_alternating_hyperparameters_follow_the_oracle():
+    """Two optimizers with different hyperparameters step in turn through the one scratch
+    array; the step-counter-only scalars it keeps between calls belong to one of them at
+    a time, and each step must still match the oracle bit for bit."""
+    import oracle
+    n, nd = 8200, 4
+    gen = torch.Generator().manual_seed(11)
+    users = []
+    for hp in (dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01),
+               dict(lr=3e-4, beta1=0.5, beta2=0.95, eps=1e-6, weight_decay=0.0)):
+        master = (torch.randn(n, generator=gen) * 0.02).float()
+        users.append({"hp": hp, "master": master.cuda(), "m": torch.zeros(n, device="cuda"),
+                      "v": torch.zeros(n, device="cuda"),
+                      "p16": master.half().cuda(),
+                      "counter": torch.zeros(1, dtype=torch.int64, device="cuda"),
+                      "ref": [master.numpy().copy(), np.zeros(n, np.float32),
+                              np.zeros(n, np.float32),
+                              master.half().numpy().view(np.uint16).copy()],
+                      "t": 0})
+    for rnd in range(3):
+        for u in users:
+            g = [(torch.randn(n, generator=gen) * 1e-3 * 1024).half() for _ in range(nd)]
+            z.zero_shard_step_noalloc(nd, n, n, [x.cuda() for x in g], u["master"], u["m"],
+                                      u["v"], u["p16"], u["counter"], u["hp"], 1024.0, 0.1)
+            sc = oracle.step([x.numpy().view(np.uint16) for x in g], *u["ref"], 1024.0, 0.1,
+                             oracle.Hyper(**u["hp"]), u["t"])
+            u["t"] = sc.step
+            torch.cuda.synchronize()
+            assert int(u["counter"].item()) == sc.step == rnd + 1
+            for a, b in zip((u["master"], u["m"], u["v"]), u["ref"][:3]):
+                assert np.array_equal(f32(a).view(np.uint32), b.view(np.uint32)), rnd
+            assert np.array_equal(h16(u["p16"]), u["ref"][3]), rnd
+
+
 def test_noalloc_refuses_spans_beyond_its_array():
     fake = [0x10000 + 0x1000 * k for k in range(4)]
     n = z.ZERO_NOALLOC_MAX_SPAN + 8
