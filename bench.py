@@ -461,27 +461,23 @@ def run_ours(args, w0):
         one_step(gsets[i % len(gsets)])
     barrier()
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    z.zero_profile_read(plan, reset=True)
-    z.zero_profile_enable(plan, True)
-    barrier()
     # A working set that L2 could hold between steps (the gradient sets and the state)
     # gets an L2 flush before every step: a write of twice the L2 size, outside the step's
     # own events; the step time is then the sum of the per-step event intervals.
     flush_buf = (torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
                  if l2_flush(w0) else None)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks.mark("start")
-    if flush_buf is None:
-        e0.record(stream)
-        for i in range(args.steps):
-            one_step(gsets[i % len(gsets)])
-        e1.record(stream)
+
+    def timed_steps():
+        """K steps between events on the launching stream; returns milliseconds."""
         barrier()
-        ms_total = e0.elapsed_time(e1)
-    else:
+        if flush_buf is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                one_step(gsets[i % len(gsets)])
+            e1.record(stream)
+            barrier()
+            return e0.elapsed_time(e1)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         # hold the stream for a moment so that the host queues the steps ahead of the GPU:
@@ -493,7 +489,20 @@ def run_ours(args, w0):
             one_step(gsets[i % len(gsets)])
             ev[i][1].record(stream)
         barrier()
-        ms_total = sum(a.elapsed_time(b) for a, b in ev)
+        return sum(a.elapsed_time(b) for a, b in ev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    # Timed region 1, the step as a user runs it: the step time and `value`.
+    # Timed region 2, the same K steps with the library's per-launch events on: each
+    # kernel's average duration (the roofline). The events themselves add a few
+    # microseconds per step, which is why the step time is taken without them.
+    clocks.mark("start")
+    ms_total = timed_steps()
+    z.zero_profile_read(plan, reset=True)
+    z.zero_profile_enable(plan, True)
+    ms_profiled = timed_steps() if graphs is None else None  # replays carry no events
     clocks.mark("end")
     z.zero_profile_enable(plan, False)
     kms, klaunch = z.zero_profile_read(plan, reset=True)
@@ -559,12 +568,15 @@ def run_ours(args, w0):
         name, alg_bytes = kinds[dom]
         avg_ms = kms[dom] / klaunch[dom]
         achieved = alg_bytes / (avg_ms / 1e3) / 1e9
-        traffic = load_traffic(name, w)
+        # the stored captures are of HBM-resident state
+        traffic = load_traffic(name, w) if args.state != "host" else None
         roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                     "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
                     "avg_launch_ms": avg_ms,
-                    "time_share": {kinds[k][0]: kms[k] / sum(kms[:3]) for k in kinds if klaunch[k]}}
+                    "time_share": {kinds[k][0]: kms[k] / sum(kms[:3]) for k in kinds if klaunch[k]},
+                    "events": "per-launch events of a second timed pass of the same K steps; "
+                              f"that pass took {ms_profiled / args.steps:.4f} ms/step"}
         launches = int(sum(klaunch[:3])) * world
     else:
         # replays carry no per-launch events: the roofline is taken over the whole step
@@ -583,6 +595,9 @@ def run_ours(args, w0):
         return 0
     cpu = oracle_sample_rate(w0, args.cpu_seconds) if args.cpu_seconds > 0 else None
     cfg = config_of(w0, world)
+    cfg["timing"] = ("K steps between two events on the launching stream, without the "
+                     "library's per-launch events (a second pass with them gives the "
+                     "per-kernel durations)")
     if graphs is not None:
         cfg["launch"] = "CUDA graph replay (one graph per gradient set)"
     if args.state == "host":
