@@ -516,37 +516,61 @@ def run_ours(args, w0):
     total_params = w0.span()[2]
     value = total_params / (ms_per_step / 1e3)
 
-    # e2e through the public API with host buffers: per step the H2D copy of the step's
-    # gradients from pinned host memory, the step, and the D2H read of its result
-    # e2e through the public API with host buffers. Two ways a user can feed the step
-    # from pinned host memory, each timed per step including the read-back of the step's
-    # result: "copy" stages the gradients into HBM with cudaMemcpyAsync first; "zero_copy"
-    # passes the pinned host pointers to the step, whose reduce kernel reads them over
-    # NVLink-C2C directly.
+    # e2e through the public API with host buffers. Three ways a user can feed the step
+    # from pinned host memory, each timed over whole steps, every step including the
+    # upload of its own gradients and the read-back of its result: "copy" stages the
+    # gradients into HBM with cudaMemcpyAsync and then steps; "copy_overlap" does the same
+    # through two device buffers, uploading step i+1's gradients on a second stream while
+    # step i runs; "zero_copy" passes the pinned host pointers to the step, whose reduce
+    # kernel reads them over NVLink-C2C directly.
     e2e_steps = 0
     e2e_modes = {}
     if not args.no_e2e:
         host = [[g.cpu().pin_memory() for g in gs] for gs in gsets]
-        dev_g = [torch.empty_like(g) for g in gsets[0]]
+        dev_g = [[torch.empty_like(g) for g in gsets[0]] for _ in range(2)]
         e2e_steps = max(3, min(args.steps, 100))
+        copy_stream = torch.cuda.Stream()
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step(i, mode):
-            hs = host[i % len(host)]
-            if mode == "copy":
-                for d, h in zip(dev_g, hs):
-                    d.copy_(h, non_blocking=True)
-                one_step(dev_g)
-            else:
-                one_step(hs)
-            z.zero_step_result(plan)
+        def upload(i, buf):  # step i's gradients into buf, on the current stream
+            for d, h in zip(buf, host[i % len(host)]):
+                d.copy_(h, non_blocking=True)
 
-        for mode in ("copy", "zero_copy"):
-            for i in range(2):
-                e2e_step(i, mode)
+        def run_mode(mode, n):
+            """n steps of `mode`, from the first upload to the last result read."""
+            if mode == "copy_overlap":
+                # buffer b = i % 2: upload i waits until step i-2 has consumed buffer b
+                with torch.cuda.stream(copy_stream):
+                    upload(0, dev_g[0])
+                    uploaded[0].record(copy_stream)
+                for i in range(n):
+                    b = i % 2
+                    if i + 1 < n:
+                        nb = (i + 1) % 2
+                        with torch.cuda.stream(copy_stream):
+                            if i >= 1:
+                                copy_stream.wait_event(consumed[nb])
+                            upload(i + 1, dev_g[nb])
+                            uploaded[nb].record(copy_stream)
+                    stream.wait_event(uploaded[b])
+                    one_step(dev_g[b])
+                    consumed[b].record(stream)
+                    z.zero_step_result(plan)
+                return
+            for i in range(n):
+                if mode == "copy":
+                    upload(i, dev_g[0])
+                    one_step(dev_g[0])
+                else:
+                    one_step(host[i % len(host)])
+                z.zero_step_result(plan)
+
+        for mode in ("copy", "copy_overlap", "zero_copy"):
+            run_mode(mode, 2)
             barrier()
             t0 = time.perf_counter()
-            for i in range(e2e_steps):
-                e2e_step(i, mode)
+            run_mode(mode, e2e_steps)
             barrier()
             sec = torch.tensor([(time.perf_counter() - t0) / e2e_steps], dtype=torch.float64,
                                device=dev)
