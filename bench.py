@@ -435,8 +435,11 @@ def run_ours(args, w0):
     if args.graph and dist is None:
         # one captured step per gradient set: a replay launches both kernels at once,
         # which removes the per-launch host cost that dominates small spans
+        z.zero_profile_enable(plan, True)
         one_step(gsets[0])
         torch.cuda.synchronize()
+        z.zero_profile_enable(plan, False)
+        launches_per_step = int(sum(z.zero_profile_read(plan, reset=True)[1][:3]))
         graphs = []
         for gs in gsets:
             g = torch.cuda.CUDAGraph()
@@ -586,7 +589,7 @@ def run_ours(args, w0):
     n_real = n_valid
     kinds = {0: ("reduce", (2 * w.nd + 4) * n_span),
              1: ("update", 30 * n_real),
-             2: ("finalize", 0)}
+             2: ("scalars", 0)}
     if graphs is None:
         dom = max((k for k in kinds if klaunch[k]), key=lambda k: kms[k])
         name, alg_bytes = kinds[dom]
@@ -610,7 +613,7 @@ def run_ours(args, w0):
                     "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
                     "alg_bytes_per_launch": alg_bytes, "avg_launch_ms": ms_per_step}
-        launches = 2 * args.steps * world
+        launches = launches_per_step * args.steps * world
     step_alg = (2 * w0.nd + 26) * total_params
     step_gbs = step_alg / (ms_per_step / 1e3) / 1e9
     moved = (2 * w0.nd + 34) * total_params / (ms_per_step / 1e3) / 1e9

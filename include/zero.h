@@ -159,12 +159,16 @@ int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float
  * 0..nd-1 (the reduce-scatter's arithmetic), the overflow flag and the norm over the
  * span's real parameters, and, unless the flag is set, the AdamW update of master,
  * exp_avg and exp_avg_sq with the fp16 cast into param16; the step counter advances
- * only on an applied step. Enqueued on stream; no host synchronisation. The two kernel
- * launches it makes contain no host-side decision, so the call can be captured in a
- * CUDA graph and replayed (the graph keeps the pointers it was captured with); make one
- * ordinary call on the device first, so that the kernels' one-time per-device set-up
- * happens outside the capture. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EUNBOUND,
- * ZERO_ECUDA. */
+ * only on an applied step. Enqueued on stream; no host synchronisation. When the span
+ * fills at least one wave of the reduce, a one-thread kernel computing the next step's
+ * step-counter-only scalars runs on a second stream that the plan owns, forked from
+ * `stream` after the reduce and joined back into it after the update (stream order for
+ * the caller is unchanged). The launches contain no host-side decision, so the call can
+ * be captured in a CUDA graph and replayed (the graph keeps the pointers it was captured
+ * with); make one ordinary call on the device first, so that the kernels' one-time
+ * per-device set-up happens outside the capture (the plan's second stream is made when
+ * state is bound).
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_EUNBOUND, ZERO_ECUDA. */
 int zero_shard_step(zero_plan* plan, int32_t r0, int32_t r1, const void* const* grad_ptrs,
                     float loss_scale, float clip, void* stream);
 
@@ -228,7 +232,8 @@ int zero_memory_bytes(int64_t n_params, int32_t nd, int32_t align, int32_t stage
 /* Kernel timing with CUDA events on the launching stream, for profiling (a measurement
  * facility; the pages have no counterpart). When enabled,
  * every kernel the plan launches is bracketed by two events; zero_profile_read
- * synchronises and returns, per kernel kind (0 reduce, 1 update, 2 finalize, 3 gather),
+ * synchronises and returns, per kernel kind (0 reduce, 1 update, 2 scalars: the
+ * finalize of a split step and the next step's step-counter-only scalars, 3 gather),
  * the summed milliseconds and the launch count, then clears them if reset != 0. Off by
  * default. Errors: ZERO_EINVAL, ZERO_ECUDA. */
 #define ZERO_PROF_KINDS 4

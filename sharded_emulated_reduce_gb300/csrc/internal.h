@@ -109,7 +109,12 @@ struct GatherLaunch {
 constexpr int64_t kGatherTile = 32768;  // elements per gather tile (64 KiB)
 constexpr int32_t kStatusGatherWait = 4;
 
-cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s);
+// *spare_cta (if given) is set to 1 when the launch carried the spare CTA that computes
+// the next step's t-only scalars (spans below one wave), else 0.
+cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta = nullptr);
+// One thread: the t-only scalars for the step counter now in the scratch, into their slot
+// (a no-op when the slot holds them already).
+cudaError_t launch_next_scalars(DevScratch* scratch, const HostHParams& hp, cudaStream_t s);
 cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,
                             const HostHParams& hp, cudaStream_t s);
 cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s);

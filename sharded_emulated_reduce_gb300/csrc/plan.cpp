@@ -68,6 +68,10 @@ struct zero_plan {
   zero::DevScalars* host_sc = nullptr;  // pinned
   cudaStream_t last_stream = nullptr;    // stream of the last step (zero_step_result)
   cudaStream_t gather_stream = nullptr;  // stream of the last gather (zero_gather_status)
+  // second stream for the next step's t-only scalars, forked after a full-wave reduce
+  // and joined before the caller's stream goes on
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   bool stepped = false;
 
   bool scaler_on = false;  // host mirror of the device scaler's on/off switch
@@ -177,9 +181,26 @@ int ensure_scratch(zero_plan* p, int dev) {
     cudaFree(sc);
     return cuda_fail(e, "cudaMallocHost");
   }
+  // the second stream for the next step's t-only scalars, made here (outside any graph
+  // capture the caller may start later)
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    if (ev_fork) cudaEventDestroy(ev_fork);
+    if (side) cudaStreamDestroy(side);
+    cudaFreeHost(hs);
+    cudaFree(sc);
+    return cuda_fail(e, "second stream");
+  }
   p->scratch = sc;
   p->host_sc = hs;
   p->device = dev;
+  p->side = side;
+  p->ev_fork = ev_fork;
+  p->ev_join = ev_join;
   return ZERO_OK;
 }
 
@@ -190,7 +211,7 @@ int64_t n_valid_of_span(const zero_plan* p) {
 }
 
 int do_reduce(zero_plan* p, const void* const* grads, bool finalize, float loss_scale,
-              float clip, cudaStream_t s) {
+              float clip, cudaStream_t s, int* spare_cta = nullptr) {
   // contributions are span-relative: element i of rank k is flat index r0*S + i
   zero::ReduceLaunch rl{};
   rl.grads = grads;
@@ -206,9 +227,31 @@ int do_reduce(zero_plan* p, const void* const* grads, bool finalize, float loss_
   rl.grid = 0;
   EventPair ev;
   prof_begin(p, s, &ev);
-  cudaError_t e = zero::launch_reduce(rl, s);
+  cudaError_t e = zero::launch_reduce(rl, s, spare_cta);
   prof_end(p, s, &ev, 0);
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  return ZERO_OK;
+}
+
+// The next step's t-only scalars on the plan's second stream: forked from s after the
+// reduce (whose combine has advanced the step counter), joined back into s after the
+// update, so the next operation on s finds them done. They run while the update runs.
+int fork_next_scalars(zero_plan* p, cudaStream_t s) {
+  cudaError_t e = cudaEventRecord(p->ev_fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->ev_fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "fork");
+  EventPair ev;
+  prof_begin(p, p->side, &ev);
+  e = zero::launch_next_scalars(p->scratch, p->hp, p->side);
+  prof_end(p, p->side, &ev, 2);
+  if (e == cudaSuccess) e = cudaEventRecord(p->ev_join, p->side);
+  if (e != cudaSuccess) return cuda_fail(e, "next-step scalars");
+  return ZERO_OK;
+}
+
+int join_next_scalars(zero_plan* p, cudaStream_t s) {
+  cudaError_t e = cudaStreamWaitEvent(s, p->ev_join, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "join");
   return ZERO_OK;
 }
 
@@ -282,6 +325,9 @@ void zero_plan_destroy(zero_plan* p) {
     cudaEventDestroy(e.start);
     cudaEventDestroy(e.stop);
   }
+  if (p->side) cudaStreamDestroy(p->side);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
   if (p->scratch) cudaFree(p->scratch);
   if (p->host_sc) cudaFreeHost(p->host_sc);
   if (has_dev && prev != p->device) cudaSetDevice(prev);
@@ -347,9 +393,15 @@ int zero_shard_step(zero_plan* p, int32_t r0, int32_t r1, const void* const* gra
   if (!rc) rc = check_device(p);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = do_reduce(p, grads, true, loss_scale, clip, s);
+  int spare = 0;
+  rc = do_reduce(p, grads, true, loss_scale, clip, s, &spare);
+  if (rc) return rc;
+  // a full-wave reduce has no spare CTA for the next step's t-only scalars
+  const bool side = !spare;
+  if (side) rc = fork_next_scalars(p, s);
   if (rc) return rc;
   rc = do_update(p, s);
+  if (!rc && side) rc = join_next_scalars(p, s);
   if (rc) return rc;
   p->last_stream = s;
   p->stepped = true;

@@ -117,28 +117,26 @@ __device__ __forceinline__ bool pre_matches(const DevPre* p, long long t, const 
 }
 
 // The step's scalars from its statistics (one thread). Double arithmetic, each
-// operation rounded to nearest, then one rounding to fp32. With CACHED, the t-only
-// scalars come from slot t & 1 when its tag matches (else they are computed here);
-// without, they are computed here.
-template <bool CACHED>
+// operation rounded to nearest, then one rounding to fp32. The t-only scalars come from
+// slot t & 1 when its tag matches; otherwise they are computed here, inline with
+// INLINE (the full-wave reduce, whose code generation is tuned with it) or as a call.
+template <bool INLINE>
 __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float loss_scale_arg,
                                 float clip, const HostHParams& hp) {
   DevScalars sc;
   const long long t = st->step;
   DevPre pre;
-  if constexpr (CACHED) {
-    const DevPre* slot = &st->pre[t & 1];
-    if (pre_matches(slot, t, hp)) {
-      pre.omb1 = __ldcg(&slot->omb1);
-      pre.omb2 = __ldcg(&slot->omb2);
-      pre.bc1 = __ldcg(&slot->bc1);
-      pre.bc2 = __ldcg(&slot->bc2);
-      pre.decay = __ldcg(&slot->decay);
-    } else {
-      pre = pre_scalars_call(t, hp);
-    }
-  } else {
+  const DevPre* slot = &st->pre[t & 1];
+  if (pre_matches(slot, t, hp)) {
+    pre.omb1 = __ldcg(&slot->omb1);
+    pre.omb2 = __ldcg(&slot->omb2);
+    pre.bc1 = __ldcg(&slot->bc1);
+    pre.bc2 = __ldcg(&slot->bc2);
+    pre.decay = __ldcg(&slot->decay);
+  } else if constexpr (INLINE) {
     pre = pre_scalars(t, hp);
+  } else {
+    pre = pre_scalars_call(t, hp);
   }
   // with the dynamic scaler on, the gradients carry the device-resident scale
   DevScaler scaler = st->scaler;
@@ -273,7 +271,8 @@ __device__ __forceinline__ void sum_group(const ReduceArgs<CAP>& a, long long v,
 // no part in the combine, which then finds this step's in slot t & 1. The other CTAs
 // reduce; the last of them to finish combines their partials.
 template <int ND, int CAP, bool PRE>
-__global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ ReduceArgs<CAP> a) {
+__global__ void __launch_bounds__(kThreads, (ND >= 32) ? 5 : 0)
+    k_reduce(const __grid_constant__ ReduceArgs<CAP> a) {
   DevScratch* st = a.st;
   if constexpr (PRE) {
     if (blockIdx.x == 0) {
@@ -344,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Red
     st->stats[3] = (long long)(tot.hi & 0xffffffffull);
     st->stats[4] = (long long)(tot.hi >> 32);
     st->stats[5] = st->stats[6] = st->stats[7] = 0;
-    if (a.finalize) compute_scalars<PRE>(st, tb, tot, a.loss_scale, a.clip, a.hp);
+    if (a.finalize) compute_scalars<!PRE>(st, tb, tot, a.loss_scale, a.clip, a.hp);
     st->ticket = 0;
   }
 }
@@ -363,7 +362,16 @@ __global__ void k_finalize(DevScratch* st, float loss_scale, float clip, HostHPa
       default: add128(ss, 0ull, l << 32); break;
     }
   }
-  compute_scalars<true>(st, bad, ss, loss_scale, clip, hp);
+  compute_scalars<false>(st, bad, ss, loss_scale, clip, hp);
+}
+
+// The t-only scalars for the counter now in the scratch (the next step's), off the
+// step's critical path: launched on a second stream while the update runs.
+__global__ void k_next_scalars(DevScratch* st, HostHParams hp) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const long long t = st->step;
+  DevPre* slot = &st->pre[t & 1];
+  if (!pre_matches(slot, t, hp)) *slot = pre_scalars_call(t, hp);
 }
 
 struct UpdateArgs {
@@ -571,7 +579,7 @@ int occupancy_grid(K kernel, long long work_items, int (&per_sm)[kMaxDevices],
 }
 
 template <int ND, int CAP>
-cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s) {
+cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
   ReduceArgs<CAP> a;
   for (int r = 0; r < CAP; ++r) a.g[r] = r < p.nd ? p.grads[r] : nullptr;
   a.gsum = p.gsum;
@@ -592,6 +600,7 @@ cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s) {
   int grid = occupancy_grid(k_reduce<ND, CAP, false>, a.n_vec, occ_cache, &resident);
   if (p.grid > 0 && p.grid < grid) grid = p.grid;
   if (grid > kMaxPartialBlocks) grid = kMaxPartialBlocks;
+  if (spare_cta) *spare_cta = grid < resident ? 1 : 0;
   if (grid < resident)
     k_reduce<ND, CAP, true><<<grid + 1, kThreads, 0, s>>>(a);
   else
@@ -601,19 +610,24 @@ cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s) {
+cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
   switch (p.nd) {
-    case 1: return go_reduce<1, 16>(p, s);
-    case 2: return go_reduce<2, 16>(p, s);
-    case 4: return go_reduce<4, 16>(p, s);
-    case 8: return go_reduce<8, 16>(p, s);
-    case 16: return go_reduce<16, 16>(p, s);
-    case 32: return go_reduce<32, 64>(p, s);
-    case 64: return go_reduce<64, 64>(p, s);
+    case 1: return go_reduce<1, 16>(p, s, spare_cta);
+    case 2: return go_reduce<2, 16>(p, s, spare_cta);
+    case 4: return go_reduce<4, 16>(p, s, spare_cta);
+    case 8: return go_reduce<8, 16>(p, s, spare_cta);
+    case 16: return go_reduce<16, 16>(p, s, spare_cta);
+    case 32: return go_reduce<32, 64>(p, s, spare_cta);
+    case 64: return go_reduce<64, 64>(p, s, spare_cta);
     default:
-      if (p.nd <= 64) return go_reduce<0, 64>(p, s);
-      return go_reduce<0, ZERO_MAX_ND>(p, s);
+      if (p.nd <= 64) return go_reduce<0, 64>(p, s, spare_cta);
+      return go_reduce<0, ZERO_MAX_ND>(p, s, spare_cta);
   }
+}
+
+cudaError_t launch_next_scalars(DevScratch* scratch, const HostHParams& hp, cudaStream_t s) {
+  k_next_scalars<<<1, 32, 0, s>>>(scratch, hp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,

@@ -156,6 +156,23 @@ def test_profile_counts_every_launch():
     assert n[:3] == [6, 6, 1] and all(x > 0 for x in ms[:3])
     ms, n = z.zero_profile_read(plan)
     assert n == [0, 0, 0, 0]
+    plan.close()
+
+
+def test_profile_counts_the_next_step_scalars_of_a_full_wave_span():
+    # a span that fills the reduce's wave computes the next step's scalars in a one-thread
+    # kernel on the plan's second stream: one more launch of kind 2 per step
+    w = small(n=3_000_000, nd=4, cfg=211, steps=1)
+    master, m, v, p16, ws = wl.make_state(w)
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, 0, 4, master, m, v, p16, ws, 0)
+    z.zero_profile_enable(plan, True)
+    grads = wl.make_grads(w, 0)
+    for _ in range(3):
+        z.zero_shard_step(plan, 0, 4, grads, w.loss_scale, w.clip)
+    ms, n = z.zero_profile_read(plan, reset=True)
+    assert n[:3] == [3, 3, 3]
+    plan.close()
 
 
 def test_step_counter_continues_from_initial_step():
@@ -242,10 +259,14 @@ def test_dist_step_in_one_process_group_equals_step():
         dist.destroy_process_group()
 
 
-def test_step_captured_in_a_cuda_graph_matches_eager_steps():
-    # the step's two launches make no host-side decision, so they can be captured once and
-    # replayed; replays must give the same bits as eager calls (including an overflow skip)
-    w = small(n=300_001, nd=8, r1=8, cfg=250, steps=4, inject=((2, 3, wl.POS_INF, 4321),))
+@pytest.mark.parametrize("n", [300_001, 3_000_001])
+def test_step_captured_in_a_cuda_graph_matches_eager_steps(n):
+    # the step's launches make no host-side decision, so they can be captured once and
+    # replayed; replays must give the same bits as eager calls (including an overflow
+    # skip). 300,001 parameters need less than one wave of the reduce (its spare CTA
+    # computes the next step's scalars); 3,000,001 fill it, and the capture then holds
+    # the fork to the plan's second stream, its one-thread kernel and the join.
+    w = small(n=n, nd=8, r1=8, cfg=250, steps=4, inject=((2, 3, wl.POS_INF, 4321),))
     first, n_span, n_valid = w.span()
     results = []
     for graph in (False, True):
