@@ -1,0 +1,79 @@
+"""The bench's one-line JSON output: the keys and types every line must carry.
+
+The reference arm (the oracle on the host cores) runs here on the CPU; the GPU lines (the
+shard step with its end-to-end, roofline, CPU-baseline and clock objects, and the
+gather) run with a few steps on a GPU."""
+import contextlib
+import io
+import json
+
+import pytest
+
+import bench
+
+COMMON = {"metric": str, "value": float, "unit": str, "n_gpus": int, "steps": int,
+          "warmup": int, "ms_per_step": float, "higher_is_better": bool, "scaling": str,
+          "dtype": str, "data": str, "config": dict}
+
+
+def run(argv):
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        rc = bench.main(argv)
+    assert rc == 0
+    lines = [l for l in out.getvalue().splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+def check_common(d):
+    for k, t in COMMON.items():
+        assert isinstance(d[k], t), k
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["vs_baseline"] is None
+    assert isinstance(d["config"]["workload"], str)
+
+
+def check_cpu_baseline(c):
+    assert c["kind"] == "oracle" and c["value"] > 0 and c["cores"] >= 1
+    assert isinstance(c["unit"], str) and isinstance(c["sample"], str)
+
+
+def test_reference_arm_line():
+    d = run(["--impl", "reference", "--workload", "zero2_tiny_1m_nd4", "--steps", "2",
+             "--warmup", "3"])
+    check_common(d)
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
+    check_cpu_baseline(d["cpu_baseline"])
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.gpu
+def test_step_line():
+    d = run(["--workload", "zero2_tiny_1m_nd4", "--steps", "20", "--warmup", "3",
+             "--cpu-seconds", "1"])
+    check_common(d)
+    assert d["unit"] == "params/s" and d["higher_is_better"] is True
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 2 * 1048576
+    assert e["d2h_bytes_per_step"] > 0 and set(e["by_mode"]) == {"copy", "copy_overlap",
+                                                                  "zero_copy"}
+    assert d["gpu_launches"] >= 2 * 20
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    check_cpu_baseline(d["cpu_baseline"])
+    c = d["clocks"]
+    assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
+    assert d["last_step"]["skipped"] == 0
+
+
+@pytest.mark.gpu
+def test_gather_line():
+    d = run(["--op", "gather", "--workload", "zero3_1p3b_rank0_nd64", "--steps", "3",
+             "--warmup", "3", "--cpu-seconds", "0.5"])
+    check_common(d)
+    assert d["gpu_launches"] == 3 and d["roofline"]["kernel"] == "gather"
+    check_cpu_baseline(d["cpu_baseline"])
