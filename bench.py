@@ -708,8 +708,14 @@ def run_gather(args, w):
            for l in range(len(offs) - 1)]
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
     stream = torch.cuda.current_stream()
+
+    def gather():
+        if args.prefetch:  # one launch and one event per layer
+            return z.zero_prefetch_layers(plan, offs, shards, dst, stream)
+        return z.zero_gather_layers(plan, offs, shards, dst, stream)
+
     for _ in range(args.warmup):
-        z.zero_gather_layers(plan, offs, shards, dst, stream)
+        gather()
     torch.cuda.synchronize()
     clocks = ClockSampler(0)
     clocks.start()
@@ -719,12 +725,23 @@ def run_gather(args, w):
     clocks.mark("start")
     e0.record(stream)
     for _ in range(args.steps):
-        z.zero_gather_layers(plan, offs, shards, dst, stream)
+        gather()
     e1.record(stream)
     torch.cuda.synchronize()
     clocks.mark("end")
+    kms, kl = z.zero_profile_read(plan, reset=True)  # the timed calls only
+    z.zero_profile_enable(plan, False)
+    prefetch = None
+    if args.prefetch:
+        # when each layer is ready, counted from the call (one more call, after the timing)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        evs = z.zero_prefetch_layers(plan, offs, shards, dst, stream, timing=True)
+        torch.cuda.synchronize()
+        ready = [t0.elapsed_time(e) for e in evs]
+        prefetch = {"layer_ready_ms": ready, "first_layer_ms": ready[0],
+                    "all_layers_ms": ready[-1]}
     ms = e0.elapsed_time(e1) / args.steps
-    kms, kl = z.zero_profile_read(plan, reset=True)
     clk = clocks.stop()
     n_moved = offs[-1] - offs[0]
     peak, peak_kind = load_peaks()
@@ -739,20 +756,23 @@ def run_gather(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
         "vs_baseline": None, "dtype": "f16 (copy)", "data": "synthetic",
         "config": {"workload": w.name, "op": "gather", "n_params": w.n, "nd": w.nd,
-                   "layer_shift": args.layer_shift,
+                   "layer_shift": args.layer_shift, "prefetch": bool(args.prefetch),
                    "layers": len(offs) - 1, "shard_len": s,
                    "l2": f"inputs larger than L2 ({2 * w.n / 1e9:.1f} GB of shards); no flush"},
         "e2e": None, "gpu_launches": int(kl[z.PROF_GATHER]),
         "roofline": {"bound": "hbm", "kernel": "gather", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                     # the stored capture is of aligned layer boundaries
-                     "traffic": None if args.layer_shift else load_traffic("gather", w),
+                     # the stored capture is of one aligned whole-buffer launch
+                     "traffic": (None if args.layer_shift or args.prefetch
+                                 else load_traffic("gather", w)),
                      "alg_bytes_per_launch": alg,
                      "avg_launch_ms": avg},
         "cpu_baseline": (gather_cpu_rate(w, args.cpu_seconds) if args.cpu_seconds > 0
                          else None),
         "clocks": clk,
     }
+    if prefetch is not None:
+        line["prefetch"] = prefetch
     print(json.dumps(line))
     plan.close()
     return 0
@@ -774,6 +794,8 @@ def main(argv=None):
     ap.add_argument("--state", default="device", choices=["device", "host"],
                     help="where master/m/v/param16 live: HBM, or pinned Grace memory read "
                          "and written over NVLink-C2C")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="gather: one launch and one event per layer (zero_prefetch_layers)")
     ap.add_argument("--layer-shift", type=int, default=0,
                     help="gather: shift interior layer boundaries by this many elements")
     ap.add_argument("--graph", action="store_true",

@@ -433,12 +433,13 @@ def torch_uint8():
 
 def zero_prefetch_layers(plan: Plan, layer_offsets: Sequence[int], shards: Sequence,
                          layer_dst: Sequence, stream=None, first: int = 0,
-                         count: int | None = None) -> list:
+                         count: int | None = None, timing: bool = False) -> list:
     """Gather layers ``first .. first+count-1`` one launch each on ``stream`` and return one
-    torch.cuda.Event per layer, recorded right after that layer's copy. A consumer stream
-    that waits on event l can start on layer l while later layers are still being
-    gathered: the "dynamic communication schedule" of the ZeRO method entry, in which the
-    all-gather of the next layers runs ahead of the work on the current one."""
+    torch.cuda.Event per layer, recorded right after that layer's copy (with ``timing``,
+    events that can be timed). A consumer stream that waits on event l can start on layer
+    l while later layers are still being gathered: the "dynamic communication schedule"
+    of the ZeRO method entry, in which the all-gather of the next layers runs ahead of the
+    work on the current one."""
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
     n_layers = len(layer_offsets) - 1
@@ -446,7 +447,7 @@ def zero_prefetch_layers(plan: Plan, layer_offsets: Sequence[int], shards: Seque
     events = []
     for l in range(first, last):
         zero_gather_layers(plan, layer_offsets[l:l + 2], shards, [layer_dst[l]], s)
-        ev = torch.cuda.Event()
+        ev = torch.cuda.Event(enable_timing=timing)
         ev.record(s)
         events.append(ev)
     return events

@@ -77,3 +77,14 @@ def test_gather_line():
     check_common(d)
     assert d["gpu_launches"] == 3 and d["roofline"]["kernel"] == "gather"
     check_cpu_baseline(d["cpu_baseline"])
+
+
+@pytest.mark.gpu
+def test_gather_prefetch_line():
+    d = run(["--op", "gather", "--workload", "zero3_1p3b_rank0_nd64", "--steps", "3",
+             "--warmup", "3", "--cpu-seconds", "0", "--prefetch"])
+    check_common(d)
+    layers = d["config"]["layers"]
+    assert d["gpu_launches"] == 3 * layers
+    ready = d["prefetch"]["layer_ready_ms"]
+    assert len(ready) == layers and ready == sorted(ready) and ready[0] < ready[-1]
