@@ -322,14 +322,20 @@ def gather_cpu_rate(w, seconds: float):
     threads = host_threads()
     _, s = w.layout()
     s_small = max(8, min(s, threads * SAMPLE_PER_THREAD // w.nd) // 8 * 8)
-    offs = [o * s_small // s for o in w.layers]
-    n_layers = len(offs) - 1
+    layer_offs = [o * s_small // s for o in (w.layers or (0, w.n))]
+    n_layers = len(layer_offs) - 1
+    # cut points at the layer boundaries and at one slice per thread, so that a layout of
+    # few layers (one, for the full-buffer gather) still keeps every thread busy
+    span = layer_offs[-1] - layer_offs[0]
+    offs = sorted(set(layer_offs) | {layer_offs[0] + span * i // threads
+                                     for i in range(threads)})
+    n_pieces = len(offs) - 1
     with ThreadPoolExecutor(threads) as pool:
         shards = [_generate(lambda a, k, r=r: synth.values_f16(
                       wl.key(w, synth.SHARD16, 0, r), w.shard_sigma, r * s_small + a, k),
                       s_small, pool) for r in range(w.nd)]
-        groups = min(threads, n_layers)
-        cuts = [n_layers * i // groups for i in range(groups + 1)]
+        groups = min(threads, n_pieces)
+        cuts = [n_pieces * i // groups for i in range(groups + 1)]
         parts = [offs[cuts[i]:cuts[i + 1] + 1] for i in range(groups)]
         done = 0
         t0 = time.perf_counter()
@@ -343,8 +349,9 @@ def gather_cpu_rate(w, seconds: float):
     return {"value": moved * done / el, "unit": "params/s", "cores": groups, "kind": "oracle",
             "sample": (f"oracle.gather (C) over {w.nd} shards of {s_small:,} elements into "
                        f"{n_layers} layers ({moved:,} parameters; the workload's layer "
-                       f"offsets scaled by {s_small:,}/{s:,}), layer groups on {groups} host "
-                       f"threads; {done} passes in {el:.1f} s")}
+                       f"offsets scaled by {s_small:,}/{s:,}), cut into {n_pieces} pieces "
+                       f"at the layer boundaries and per thread, piece groups on {groups} "
+                       f"host threads; {done} passes in {el:.1f} s")}
 
 
 def run_reference(args, w):
@@ -684,7 +691,9 @@ def load_traffic(kernel: str, w):
     return None if not ent else ent.get("dram_bytes_per_launch")
 
 def run_gather(args, w):
-    """Time the ZeRO-3 gather of all Nd fp16 shards into the workload's layer buffers."""
+    """Time the gather of all Nd fp16 shards into the workload's layer buffers (ZeRO-3),
+    or, for a workload without a layer table, into one buffer holding the whole flat
+    parameter vector (the parameter all-gather of ZeRO-1/2)."""
     import torch
 
     import sharded_emulated_reduce_gb300 as z
@@ -693,13 +702,11 @@ def run_gather(args, w):
     if env_int("WORLD_SIZE", 1) > 1 and env_int("RANK", 0) != 0:
         return 0
     torch.cuda.set_device(0)
-    if not w.layers:
-        raise SystemExit(f"workload {w.name} has no layer table")
     _, s = w.layout()
     shard0 = torch.empty(s, dtype=torch.float16, device="cuda")
     shards = wl.make_shards(w, shard0)
     wl.fill(shard0, wl.key(w, wl.SHARD16, 0, 0), w.shard_sigma, start=0, n_valid=w.n)
-    offs = list(w.layers)
+    offs = list(w.layers) if w.layers else [0, w.n]  # ZeRO-1/2: one full-buffer layer
     if args.layer_shift:
         # move every interior layer boundary by a few elements: layers then start at
         # addresses misaligned (mod 16 bytes) relative to the shards they copy from

@@ -80,6 +80,15 @@ def test_gather_line():
 
 
 @pytest.mark.gpu
+def test_full_buffer_gather_line():
+    # a workload without a layer table: the ZeRO-1/2 all-gather into one flat buffer
+    d = run(["--op", "gather", "--workload", "flat_32m_nd8", "--steps", "3", "--warmup", "3",
+             "--cpu-seconds", "0"])
+    check_common(d)
+    assert d["config"]["layers"] == 1 and d["gpu_launches"] == 3
+
+
+@pytest.mark.gpu
 def test_gather_prefetch_line():
     d = run(["--op", "gather", "--workload", "zero3_1p3b_rank0_nd64", "--steps", "3",
              "--warmup", "3", "--cpu-seconds", "0", "--prefetch"])
