@@ -206,6 +206,9 @@ int zero_step_result(zero_plan* plan, zero_step_info* out);
  *   layer_dst: host array of n_layers device pointers (2-byte aligned; may be NULL for
  *     an empty layer). Destinations must not overlap the shards or each other.
  * For ZeRO-1/2 the parameter all-gather is this call with one layer [0, n_params).
+ * Each layer is cut at shard boundaries into copy segments; segments whose source and
+ * destination addresses agree modulo 16 bytes are copied by TMA bulk copies, the others
+ * by a kernel that realigns 16-byte blocks in registers (same result, same traffic).
  * Enqueued on stream. The first call on a plan that was never bound allocates the
  * plan's small device scratch (which holds the gather's status word) on the current
  * device. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */

@@ -75,6 +75,17 @@ def test_many_segments_cross_the_per_launch_table():
     run_gather(n, nd, 8, offsets)
 
 
+def test_many_segments_of_both_alignment_classes():
+    # every other boundary moved by 3 elements: aligned and misaligned segments interleave,
+    # and each of the two per-launch tables (bulk-copy kernel, realigning kernel) overflows
+    # its 128 entries within one call (about 180 segments each)
+    n, nd = 300 * 8 * 64, 64
+    step = n // 300
+    offsets = [0] + [k * step + (k % 2) * 3 for k in range(1, 300)] + [n]
+    run_gather(n, nd, 8, offsets)
+    run_gather(n, nd, 8, offsets, dst_pad=3, src_pad=1, seed=7)
+
+
 def test_prefetch_layers_with_per_layer_events():
     # producer stream gathers layer by layer; a consumer stream waits on each layer's
     # event and reads it (sum of its bits) while later layers are still being gathered
