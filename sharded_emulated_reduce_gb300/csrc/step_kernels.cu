@@ -13,6 +13,11 @@
 // vector per rank per thread, coalesced across the warp. The update streams tiles through
 // shared memory with the TMA engine's 1-D bulk copies (see k_update).
 //
+// The combine's scalars that depend only on the step counter (the bias corrections'
+// double-precision powers, slow on this part) are prepared one step ahead in a tagged
+// slot: by a spare CTA of the reduce when the span needs less than one wave, otherwise
+// by k_next_scalars, which the host runs on a second stream beside the update.
+//
 // Exactness: each summed gradient gsum is an integer multiple of 2^-24 (fp16 values
 // are, and an fp32 sum of them stays one), so k = gsum * 2^24 is an exact integer and
 // the sum of k^2 is carried exactly in 128 bits. The norm therefore does not depend on
