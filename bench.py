@@ -446,7 +446,8 @@ def run_ours(args, w0):
         one_step(gsets[0])
         torch.cuda.synchronize()
         z.zero_profile_enable(plan, False)
-        launches_per_step = int(sum(z.zero_profile_read(plan, reset=True)[1][:3]))
+        counts = z.zero_profile_read(plan, reset=True)[1]
+        launches_per_step = int(counts[0] + counts[1] + counts[2] + counts[4])
         graphs = []
         for gs in gsets:
             g = torch.cuda.CUDAGraph()
@@ -596,7 +597,8 @@ def run_ours(args, w0):
     n_real = n_valid
     kinds = {0: ("reduce", (2 * w.nd + 4) * n_span),
              1: ("update", 30 * n_real),
-             2: ("scalars", 0)}
+             2: ("scalars", 0),
+             4: ("step", 2 * w.nd * n_span + 26 * n_real)}  # small spans: one launch
     if graphs is None:
         dom = max((k for k in kinds if klaunch[k]), key=lambda k: kms[k])
         name, alg_bytes = kinds[dom]
@@ -608,10 +610,11 @@ def run_ours(args, w0):
                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                     "traffic": traffic, "alg_bytes_per_launch": alg_bytes,
                     "avg_launch_ms": avg_ms,
-                    "time_share": {kinds[k][0]: kms[k] / sum(kms[:3]) for k in kinds if klaunch[k]},
+                    "time_share": {kinds[k][0]: kms[k] / sum(kms[j] for j in kinds)
+                                   for k in kinds if klaunch[k]},
                     "events": "per-launch events of a second timed pass of the same K steps; "
                               f"that pass took {ms_profiled / args.steps:.4f} ms/step"}
-        launches = int(sum(klaunch[:3])) * world
+        launches = int(sum(klaunch[k] for k in kinds)) * world
     else:
         # replays carry no per-launch events: the roofline is taken over the whole step
         alg_bytes = (2 * w.nd + 4) * n_span + 30 * n_real

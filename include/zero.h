@@ -70,8 +70,9 @@ typedef struct {
   int32_t overflow;   /* 1 if any summed gradient in the span was inf or nan          */
   int32_t skipped;    /* 1 if the update was not applied (overflow or status != 0)    */
   int32_t status;     /* 0, or a device-side failure code: 2 = a bulk load of the
-                       * update did not arrive within its bounded wait (the update may be
-                       * partly applied; never expected on a healthy GPU)               */
+                       * update did not arrive within its bounded wait; 5 = the grid
+                       * barrier of the one-launch small-span step gave up (the update
+                       * may be partly applied; neither is expected on a healthy GPU)   */
   int32_t reserved;
   int64_t step;       /* optimizer step counter after the step                        */
   double global_norm; /* L2 norm of the unscaled summed gradient (+inf on overflow)   */
@@ -159,7 +160,10 @@ int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float
  * 0..nd-1 (the reduce-scatter's arithmetic), the overflow flag and the norm over the
  * span's real parameters, and, unless the flag is set, the AdamW update of master,
  * exp_avg and exp_avg_sq with the fp16 cast into param16; the step counter advances
- * only on an applied step. Enqueued on stream; no host synchronisation. When the span
+ * only on an applied step. Enqueued on stream; no host synchronisation. A span of at
+ * most 1024 groups of 8 parameters per SM (and nd <= 64) runs as one cooperative launch
+ * that keeps the fp32 sums in shared memory; other spans run a reduce and an update
+ * kernel. When the span
  * fills at least one wave of the reduce, a one-thread kernel computing the next step's
  * step-counter-only scalars runs on a second stream that the plan owns, forked from
  * `stream` after the reduce and joined back into it after the update (stream order for
@@ -236,10 +240,11 @@ int zero_memory_bytes(int64_t n_params, int32_t nd, int32_t align, int32_t stage
  * facility; the pages have no counterpart). When enabled,
  * every kernel the plan launches is bracketed by two events; zero_profile_read
  * synchronises and returns, per kernel kind (0 reduce, 1 update, 2 scalars: the
- * finalize of a split step and the next step's step-counter-only scalars, 3 gather),
- * the summed milliseconds and the launch count, then clears them if reset != 0. Off by
- * default. Errors: ZERO_EINVAL, ZERO_ECUDA. */
-#define ZERO_PROF_KINDS 4
+ * finalize of a split step and the next step's step-counter-only scalars, 3 gather,
+ * 4 step: a whole small-span step in one launch), the summed milliseconds and the
+ * launch count, then clears them if reset != 0. Off by default. Errors: ZERO_EINVAL,
+ * ZERO_ECUDA. */
+#define ZERO_PROF_KINDS 5
 int zero_profile_enable(zero_plan* plan, int32_t on);
 int zero_profile_read(zero_plan* plan, double* ms, int64_t* launches, int32_t reset);
 

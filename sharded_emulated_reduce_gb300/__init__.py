@@ -23,9 +23,9 @@ ZERO_ECUDA = -4
 ZERO_EDEVICE = -5
 ZERO_MAX_ND = 256
 ZERO_STATS_WORDS = 8
-ZERO_PROF_KINDS = 4
+ZERO_PROF_KINDS = 5
 ZERO_NOALLOC_MAX_SPAN = 4194304
-PROF_REDUCE, PROF_UPDATE, PROF_FINALIZE, PROF_GATHER = range(4)
+PROF_REDUCE, PROF_UPDATE, PROF_FINALIZE, PROF_GATHER, PROF_STEP = range(5)
 
 
 class ZeroError(RuntimeError):

@@ -60,6 +60,7 @@ struct DevScratch {
   long long step;       // optimizer step counter t
   unsigned int ticket;    // arrival counter of the reduce CTAs
   int32_t gather_status;  // 0, or kStatusGatherWait after a gather wait expired
+  unsigned int bar_count, bar_gen;  // grid barrier of the fused small-span step
   DevPartial partials[kMaxPartialBlocks];
 };
 
@@ -118,6 +119,17 @@ cudaError_t launch_next_scalars(DevScratch* scratch, const HostHParams& hp, cuda
 cudaError_t launch_finalize(DevScratch* scratch, float loss_scale, float clip,
                             const HostHParams& hp, cudaStream_t s);
 cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s);
+
+// The whole step as one cooperative launch, for spans of at most small_step_max_vecs()
+// groups of 8 (see k_step_small). Same arguments as the reduce plus the bound state.
+struct SmallLaunch {
+  ReduceLaunch r;  // grads, nd, n_span, n_valid, scratch, loss_scale, clip, hp (gsum unused)
+  float *master, *exp_avg, *exp_avg_sq;
+  void* param16;
+};
+long long small_step_max_vecs();  // 0 when the device cannot run it
+cudaError_t launch_small_step(const SmallLaunch& p, cudaStream_t s);
+constexpr int32_t kStatusStepWait = 5;  // the fused step's grid barrier expired
 cudaError_t launch_gather(const GatherLaunch& p, cudaStream_t s);
 
 // Set the calling thread's zero_last_error() message; returns code.

@@ -78,8 +78,8 @@ struct zero_plan {
 
   bool prof = false;
   std::vector<EventPair> free_events, pending;
-  double prof_ms[ZERO_PROF_KINDS] = {0, 0, 0, 0};
-  int64_t prof_launches[ZERO_PROF_KINDS] = {0, 0, 0, 0};
+  double prof_ms[ZERO_PROF_KINDS] = {};
+  int64_t prof_launches[ZERO_PROF_KINDS] = {};
 };
 
 namespace {
@@ -249,6 +249,38 @@ int fork_next_scalars(zero_plan* p, cudaStream_t s) {
   return ZERO_OK;
 }
 
+// The whole step as one cooperative launch, when the span is small enough for the fused
+// kernel (a graph capture records it as a cooperative kernel node).
+bool small_step_fits(const zero_plan* p) {
+  const int64_t n_vec = (int64_t)(p->r1 - p->r0) * p->s / 8;
+  return p->nd <= 64 && n_vec <= zero::small_step_max_vecs();
+}
+
+int do_small_step(zero_plan* p, const void* const* grads, float loss_scale, float clip,
+                  cudaStream_t s) {
+  zero::SmallLaunch sl{};
+  sl.r.grads = grads;
+  sl.r.nd = p->nd;
+  sl.r.gsum = nullptr;
+  sl.r.n_span = (int64_t)(p->r1 - p->r0) * p->s;
+  sl.r.n_valid = n_valid_of_span(p);
+  sl.r.scratch = p->scratch;
+  sl.r.finalize = true;
+  sl.r.loss_scale = loss_scale;
+  sl.r.clip = clip;
+  sl.r.hp = p->hp;
+  sl.master = p->master;
+  sl.exp_avg = p->exp_avg;
+  sl.exp_avg_sq = p->exp_avg_sq;
+  sl.param16 = p->param16;
+  EventPair ev;
+  prof_begin(p, s, &ev);
+  cudaError_t e = zero::launch_small_step(sl, s);
+  prof_end(p, s, &ev, 4);
+  if (e != cudaSuccess) return cuda_fail(e, "fused step launch");
+  return ZERO_OK;
+}
+
 int join_next_scalars(zero_plan* p, cudaStream_t s) {
   cudaError_t e = cudaStreamWaitEvent(s, p->ev_join, 0);
   if (e != cudaSuccess) return cuda_fail(e, "join");
@@ -393,6 +425,13 @@ int zero_shard_step(zero_plan* p, int32_t r0, int32_t r1, const void* const* gra
   if (!rc) rc = check_device(p);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (small_step_fits(p)) {
+    rc = do_small_step(p, grads, loss_scale, clip, s);
+    if (rc) return rc;
+    p->last_stream = s;
+    p->stepped = true;
+    return ZERO_OK;
+  }
   int spare = 0;
   rc = do_reduce(p, grads, true, loss_scale, clip, s, &spare);
   if (rc) return rc;
@@ -475,6 +514,12 @@ int zero_step_result(zero_plan* p, zero_step_info* out) {
   out->bc1 = sc.bc1;
   out->bc2 = sc.bc2;
   out->loss_scale = sc.loss_scale;
+  if (sc.status == zero::kStatusStepWait) {
+    // the fused step's grid barrier gave up: its arrival count may be left part-way, so
+    // start the next one from zero
+    cudaMemsetAsync(&p->scratch->bar_count, 0, 2 * sizeof(unsigned), p->last_stream);
+    cudaStreamSynchronize(p->last_stream);
+  }
   if (sc.status != 0) return fail(ZERO_EDEVICE, "device status %d", sc.status);
   return ZERO_OK;
 }

@@ -121,15 +121,12 @@ __device__ __forceinline__ bool pre_matches(const DevPre* p, long long t, const 
          __ldcg(&p->beta2) == hp.beta2 && __ldcg(&p->weight_decay) == hp.weight_decay;
 }
 
-// The step's scalars from its statistics (one thread). Double arithmetic, each
-// operation rounded to nearest, then one rounding to fp32. The t-only scalars come from
-// slot t & 1 when its tag matches; otherwise they are computed here, inline with
-// INLINE (the full-wave reduce, whose code generation is tuned with it) or as a call.
+// The t-only scalars for step counter t: from slot t & 1 when its tag matches, otherwise
+// computed here, inline with INLINE (the full-wave reduce, whose code generation is tuned
+// with it) or as a call.
 template <bool INLINE>
-__device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float loss_scale_arg,
-                                float clip, const HostHParams& hp) {
-  DevScalars sc;
-  const long long t = st->step;
+__device__ __forceinline__ DevPre t_scalars(const DevScratch* st, long long t,
+                                            const HostHParams& hp) {
   DevPre pre;
   const DevPre* slot = &st->pre[t & 1];
   if (pre_matches(slot, t, hp)) {
@@ -143,8 +140,18 @@ __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float lo
   } else {
     pre = pre_scalars_call(t, hp);
   }
+  return pre;
+}
+
+// The step's scalars from its statistics (one thread), writing nothing: t and `scaler`
+// are the step counter and loss scaler before the step, *next the scaler after it.
+// Double arithmetic, each operation rounded to nearest, then one rounding to fp32.
+__device__ __forceinline__ DevScalars make_scalars(long long t, DevScaler scaler, long long bad,
+                                                   U128 ss, float loss_scale_arg, float clip,
+                                                   const HostHParams& hp, const DevPre& pre,
+                                                   DevScaler* next) {
+  DevScalars sc;
   // with the dynamic scaler on, the gradients carry the device-resident scale
-  DevScaler scaler = st->scaler;
   const bool dynamic = scaler.interval > 0;
   const float loss_scale = dynamic ? scaler.scale : loss_scale_arg;
   sc.loss_scale = loss_scale;
@@ -178,8 +185,6 @@ __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float lo
   sc.beta1 = hp.beta1;
   sc.beta2 = hp.beta2;
   sc.eps = hp.eps;
-  st->sc = sc;
-  if (!sc.skipped) st->step = t + 1;
   if (dynamic) {
     // back off on overflow; grow after `interval` consecutive applied steps
     if (sc.overflow) {
@@ -194,8 +199,24 @@ __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float lo
       }
       scaler.good_steps = good;
     }
-    st->scaler = scaler;
   }
+  *next = scaler;
+  return sc;
+}
+
+// The step's scalars from its statistics, committed to the scratch (one thread): the
+// scalars, the step counter (advanced on an applied step) and the dynamic scaler.
+template <bool INLINE>
+__device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float loss_scale_arg,
+                                float clip, const HostHParams& hp) {
+  const long long t = st->step;
+  const DevPre pre = t_scalars<INLINE>(st, t, hp);
+  const DevScaler scaler = st->scaler;
+  DevScaler next;
+  const DevScalars sc = make_scalars(t, scaler, bad, ss, loss_scale_arg, clip, hp, pre, &next);
+  st->sc = sc;
+  if (!sc.skipped) st->step = t + 1;
+  if (scaler.interval > 0) st->scaler = next;
 }
 
 // Sum (acc, bad) over a CTA of NT threads; the result is valid in thread 0.
@@ -542,6 +563,302 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
   }
 }
 
+// ---- the fused step for small spans -------------------------------------------------
+// A span of at most kSmallVecs groups of 8 per SM runs as one cooperative launch (all
+// CTAs resident at once), one 512-thread CTA per SM, each owning a contiguous slice:
+//   1. the CTA sums its slice of the contributions in rank order into shared memory and
+//      publishes its 128-bit sum of squares and non-finite count;
+//   2. after a grid-wide barrier (bounded: it gives up after about kWaitNs and records
+//      kStatusStepWait), warp 0 of every CTA combines all the partials, the same
+//      integers in the same order, so every CTA derives the same scalars; CTA 0 commits
+//      them (and the step counter and scaler) to the scratch;
+//   3. unless the step is skipped, the CTA updates its slice from the sums it kept.
+// The fp32 sums never go to HBM and the step is one launch. The CTA's master/m/v slice
+// is brought into shared memory by bulk loads issued at the start, so it arrives while
+// the CTA reduces and waits at the barrier. A 17th warp of CTA 0
+// prepares the next step's t-only scalars meanwhile; it reads the step counter before
+// CTA 0 may advance it (named barrier 2), and the CTAs' own synchronisation uses named
+// barrier 1 over the 512 working threads only.
+constexpr int kSmallThreads = 512;
+constexpr int kSmallVecs = 1024;  // groups of 8 per CTA: 32 KiB of fp32 sums
+constexpr size_t kSmallSlice = (size_t)kSmallVecs * 8 * sizeof(float);  // one fp32 array
+constexpr size_t kSmallSmem = 4 * kSmallSlice + 16;  // sums, master, m, v, mbarrier
+constexpr unsigned kBarrierPolls = 1u << 24;
+
+template <int CAP>
+struct SmallArgs {
+  ReduceArgs<CAP> r;  // contributions, span sizes, scratch, loss scale, clip, hparams
+  float *master, *m, *v;
+  uint16_t* p16;
+  long long vecs_per_cta;
+};
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned x;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
+  return x;
+}
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Sum (acc, bad) over the CTA's kSmallThreads working threads (named barrier 1); the
+// result is valid in thread 0.
+__device__ void small_block_reduce(U128& acc, long long& bad) {
+  constexpr int W = kSmallThreads / 32;
+  __shared__ unsigned long long s_lo[W], s_hi[W];
+  __shared__ long long s_bad[W];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long lo = __shfl_xor_sync(0xffffffffu, acc.lo, o);
+    const unsigned long long hi = __shfl_xor_sync(0xffffffffu, acc.hi, o);
+    bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    add128(acc, lo, hi);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s_lo[warp] = acc.lo;
+    s_hi[warp] = acc.hi;
+    s_bad[warp] = bad;
+  }
+  bar_sync(1, kSmallThreads);
+  if (threadIdx.x == 0) {
+    U128 t{0, 0};
+    long long b = 0;
+    for (int w = 0; w < W; ++w) {
+      add128(t, s_lo[w], s_hi[w]);
+      b += s_bad[w];
+    }
+    acc = t;
+    bad = b;
+  }
+}
+
+// Grid-wide barrier of the cooperative launch (thread 0 of each CTA). The CTA's earlier
+// global writes are visible to every CTA once it returns true; false after
+// kBarrierPolls polls or about kWaitNs.
+__device__ bool grid_barrier(DevScratch* st, unsigned nblocks) {
+  const unsigned gen = ld_acquire_u32(&st->bar_gen);
+  __threadfence();
+  if (atomicAdd(&st->bar_count, 1u) == nblocks - 1) {
+    st->bar_count = 0;  // nobody touches the count again in this launch
+    __threadfence();
+    atomicAdd(&st->bar_gen, 1u);
+    return true;
+  }
+  const unsigned long long t0 = global_ns();
+  for (unsigned i = 0; i < kBarrierPolls; ++i) {
+    if (ld_acquire_u32(&st->bar_gen) != gen) {
+      __threadfence();
+      return true;
+    }
+    __nanosleep(64);
+    if ((i & 63u) == 63u && global_ns() - t0 > kWaitNs) return false;
+  }
+  return false;
+}
+
+template <int ND, int CAP>
+__global__ void __launch_bounds__(kSmallThreads + 32, 1)
+    k_step_small(const __grid_constant__ SmallArgs<CAP> a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* sums = reinterpret_cast<float*>(smem);
+  float* s_master = reinterpret_cast<float*>(smem + kSmallSlice);
+  float* s_m = reinterpret_cast<float*>(smem + 2 * kSmallSlice);
+  float* s_v = reinterpret_cast<float*>(smem + 3 * kSmallSlice);
+  uint64_t* state_bar = reinterpret_cast<uint64_t*>(smem + 4 * kSmallSlice);
+  __shared__ DevScalars s_sc;
+  __shared__ long long s_t;
+  __shared__ DevScaler s_scaler;
+  __shared__ int s_ok;
+  DevScratch* st = a.r.st;
+  const int tid = threadIdx.x;
+  if (tid >= kSmallThreads) {  // the 17th warp
+    if (blockIdx.x == 0) {
+      const long long tn = st->step + 1;  // the counter after an applied step
+      bar_arrive(2, 64);                  // CTA 0's commit waits for this read
+      if (tid == kSmallThreads) {
+        DevPre* slot = &st->pre[tn & 1];
+        if (!pre_matches(slot, tn, a.r.hp)) *slot = pre_scalars_call(tn, a.r.hp);
+      }
+    }
+    return;
+  }
+  // this CTA's slice: groups [v0, v1), real parameters [e0, e1), whole quads up to eq
+  const long long v0 = (long long)blockIdx.x * a.vecs_per_cta;
+  long long v1 = v0 + a.vecs_per_cta;
+  if (v1 > a.r.n_vec) v1 = a.r.n_vec;
+  const long long e0 = v0 * 8;
+  long long e1 = v1 * 8;
+  if (e1 > a.r.n_valid) e1 = a.r.n_valid;
+  const long long eq = e1 > e0 ? e0 + (((e1 - e0) >> 2) << 2) : e0;
+  const uint32_t state_bytes = (uint32_t)((eq - e0) * sizeof(float));  // 16-byte multiple
+  if (tid == 0) {
+    s_t = st->step;  // before this CTA arrives at the barrier, so before any commit
+    s_scaler = st->scaler;
+    if (blockIdx.x == 0) st->sc.status = 0;
+    if (state_bytes > 0) {  // the slice's state, on its way while the CTA reduces
+      mbar_init(state_bar, 1);
+      mbar_fence_init();
+      mbar_expect_tx(state_bar, 3 * state_bytes);
+      bulk_load(s_master, a.master + e0, state_bytes, state_bar);
+      bulk_load(s_m, a.m + e0, state_bytes, state_bar);
+      bulk_load(s_v, a.v + e0, state_bytes, state_bar);
+    }
+  }
+  // every exit of thread 0 from here on first lets the state loads land (bounded)
+  auto drain = [&]() { if (tid == 0 && state_bytes > 0) mbar_wait(state_bar, 0u); };
+
+  // 1. rank-order sums of this CTA's slice into shared memory, and its statistics
+  U128 acc{0, 0};
+  long long bad = 0;
+  for (long long v = v0 + tid; v < v1; v += kSmallThreads) {
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    sum_group<ND, CAP>(a.r, v, s);
+    const long long base = v * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (base + j >= a.r.n_valid) s[j] = 0.0f;  // padding: not a parameter
+      const bool fin = is_finite(s[j]);
+      bad += fin ? 0 : 1;
+      add_square(acc, fin ? s[j] : 0.0f);
+    }
+    float4* o = reinterpret_cast<float4*>(sums) + 2 * (v - v0);
+    o[0] = make_float4(s[0], s[1], s[2], s[3]);
+    o[1] = make_float4(s[4], s[5], s[6], s[7]);
+  }
+  small_block_reduce(acc, bad);
+  if (tid == 0) {
+    st->partials[blockIdx.x].lo = acc.lo;
+    st->partials[blockIdx.x].hi = acc.hi;
+    st->partials[blockIdx.x].bad = bad;
+    s_ok = grid_barrier(st, gridDim.x) ? 1 : 0;
+  }
+  bar_sync(1, kSmallThreads);
+  if (!s_ok) {
+    if (tid == 0) atomicExch(&st->sc.status, kStatusStepWait);
+    drain();
+    return;
+  }
+
+  // 2. every CTA: the same combine and the same scalars; CTA 0 commits them
+  if (tid < 32) {
+    U128 tot{0, 0};
+    long long tb = 0;
+    for (int i = tid; i < (int)gridDim.x; i += 32) {
+      const DevPartial* p = &st->partials[i];
+      add128(tot, __ldcg(&p->lo), __ldcg(&p->hi));
+      tb += __ldcg(&p->bad);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long lo = __shfl_xor_sync(0xffffffffu, tot.lo, o);
+      const unsigned long long hi = __shfl_xor_sync(0xffffffffu, tot.hi, o);
+      tb += __shfl_xor_sync(0xffffffffu, tb, o);
+      add128(tot, lo, hi);
+    }
+    DevScaler next;
+    DevScalars sc;
+    if (tid == 0) {
+      const DevPre pre = t_scalars<false>(st, s_t, a.r.hp);
+      sc = make_scalars(s_t, s_scaler, tb, tot, a.r.loss_scale, a.r.clip, a.r.hp, pre, &next);
+      s_sc = sc;
+    }
+    if (blockIdx.x == 0) {
+      bar_sync(2, 64);  // the 17th warp has read the step counter
+      if (tid == 0) {
+        st->stats[0] = tb;
+        st->stats[1] = (long long)(tot.lo & 0xffffffffull);
+        st->stats[2] = (long long)(tot.lo >> 32);
+        st->stats[3] = (long long)(tot.hi & 0xffffffffull);
+        st->stats[4] = (long long)(tot.hi >> 32);
+        st->stats[5] = st->stats[6] = st->stats[7] = 0;
+        // every field but the status word, which a CTA whose barrier expired may set
+        DevScalars* d = &st->sc;
+        d->overflow = sc.overflow;
+        d->skipped = sc.skipped;
+        d->pad = sc.pad;
+        d->step = sc.step;
+        d->ss = sc.ss;
+        d->norm = sc.norm;
+        d->clip_coef = sc.clip_coef;
+        d->s = sc.s;
+        d->omb1 = sc.omb1;
+        d->omb2 = sc.omb2;
+        d->bc1 = sc.bc1;
+        d->bc2 = sc.bc2;
+        d->decay = sc.decay;
+        d->lr = sc.lr;
+        d->beta1 = sc.beta1;
+        d->beta2 = sc.beta2;
+        d->eps = sc.eps;
+        d->loss_scale = sc.loss_scale;
+        d->pad2 = sc.pad2;
+        if (!sc.skipped) st->step = s_t + 1;
+        if (s_scaler.interval > 0) st->scaler = next;
+      }
+    }
+  }
+  bar_sync(1, kSmallThreads);
+
+  // 3. the update of this CTA's slice from the sums and state it holds
+  if (s_sc.skipped) {  // overflow: the state keeps its bits
+    drain();
+    return;
+  }
+  if (state_bytes > 0 && !mbar_wait(state_bar, 0u)) {
+    if (tid == 0) atomicExch(&st->sc.status, kStatusUpdateWait);
+    drain();
+    return;
+  }
+  Sc c;
+  c.s = s_sc.s;
+  c.b1 = s_sc.beta1;
+  c.b2 = s_sc.beta2;
+  c.omb1 = s_sc.omb1;
+  c.omb2 = s_sc.omb2;
+  c.bc1 = s_sc.bc1;
+  c.bc2 = s_sc.bc2;
+  c.eps = s_sc.eps;
+  c.decay = s_sc.decay;
+  c.lr = s_sc.lr;
+  if (e1 <= e0) return;
+  float* __restrict__ master = a.master;
+  float* __restrict__ mm = a.m;
+  float* __restrict__ vv = a.v;
+  const long long nq = (eq - e0) >> 2;  // whole quads of parameters
+  const float4* g4 = reinterpret_cast<const float4*>(sums);
+  for (long long q = tid; q < nq; q += kSmallThreads) {
+    const long long i = e0 + 4 * q;
+    const float4 g = g4[q];
+    const float4 p = reinterpret_cast<const float4*>(s_master)[q];
+    float4 m = reinterpret_cast<const float4*>(s_m)[q];
+    float4 v = reinterpret_cast<const float4*>(s_v)[q];
+    float4 r;
+    r.x = adam_elem(g.x, p.x, m.x, v.x, c);
+    r.y = adam_elem(g.y, p.y, m.y, v.y, c);
+    r.z = adam_elem(g.z, p.z, m.z, v.z, c);
+    r.w = adam_elem(g.w, p.w, m.w, v.w, c);
+    *reinterpret_cast<float4*>(master + i) = r;
+    *reinterpret_cast<float4*>(mm + i) = m;
+    *reinterpret_cast<float4*>(vv + i) = v;
+    *reinterpret_cast<uint2*>(a.p16 + i) = make_uint2(pack_h2(r.x, r.y), pack_h2(r.z, r.w));
+  }
+  if (tid < e1 - eq) {  // at most 3 parameters, at the end of the real ones
+    const long long i = eq + tid;
+    float m = mm[i], v = vv[i];
+    const float p = adam_elem(sums[i - e0], master[i], m, v, c);
+    master[i] = p;
+    mm[i] = m;
+    vv[i] = v;
+    const __half h = __float2half_rn(p);
+    a.p16[i] = *reinterpret_cast<const uint16_t*>(&h);
+  }
+}
+
 constexpr int kMaxDevices = 64;
 
 // SM count of the current device, looked up once per device.
@@ -627,6 +944,92 @@ cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta)
     default:
       if (p.nd <= 64) return go_reduce<0, 64>(p, s, spare_cta);
       return go_reduce<0, ZERO_MAX_ND>(p, s, spare_cta);
+  }
+}
+
+namespace {
+
+// The fused kernel's shared-memory limit, raised once per instantiation and device.
+template <int ND, int CAP>
+cudaError_t prepare_small() {
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(
+      k_step_small<ND, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return e;
+}
+
+template <int ND, int CAP>
+cudaError_t go_small(const SmallLaunch& p, cudaStream_t s, int sms) {
+  cudaError_t e = prepare_small<ND, CAP>();
+  if (e != cudaSuccess) return e;
+  SmallArgs<CAP> a;
+  for (int r = 0; r < CAP; ++r) a.r.g[r] = r < p.r.nd ? p.r.grads[r] : nullptr;
+  a.r.gsum = nullptr;  // the sums stay in shared memory
+  a.r.n_vec = p.r.n_span / 8;
+  a.r.n_valid = p.r.n_valid;
+  a.r.st = p.r.scratch;
+  a.r.loss_scale = p.r.loss_scale;
+  a.r.clip = p.r.clip;
+  a.r.hp = p.r.hp;
+  a.r.nd = p.r.nd;
+  a.r.finalize = 1;
+  a.master = p.master;
+  a.m = p.exp_avg;
+  a.v = p.exp_avg_sq;
+  a.p16 = static_cast<uint16_t*>(p.param16);
+  a.vecs_per_cta = (a.r.n_vec + sms - 1) / sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms);  // one CTA per SM, all resident (cooperative)
+  cfg.blockDim = dim3(kSmallThreads + 32);
+  cfg.dynamicSmemBytes = kSmallSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_step_small<ND, CAP>, a);
+}
+
+}  // namespace
+
+long long small_step_max_vecs() {
+  static long long cache[kMaxDevices] = {};
+  int dev = 0;
+  const int sms = sm_count(&dev);
+  if (dev >= 0 && dev < kMaxDevices && cache[dev] != 0) return cache[dev] > 0 ? cache[dev] : 0;
+  // every instantiation must fit one CTA per SM; the generic one holds the most registers
+  int occ = 0, occ8 = 0;
+  cudaError_t e = prepare_small<0, 64>();
+  if (e == cudaSuccess) e = prepare_small<8, 16>();
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_step_small<0, 64>,
+                                                      kSmallThreads + 32, kSmallSmem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ8, k_step_small<8, 16>,
+                                                      kSmallThreads + 32, kSmallSmem);
+  const long long v = (e == cudaSuccess && occ >= 1 && occ8 >= 1) ? (long long)sms * kSmallVecs : -1;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev] = v;
+  return v > 0 ? v : 0;
+}
+
+cudaError_t launch_small_step(const SmallLaunch& p, cudaStream_t s) {
+  const int sms = sm_count(nullptr);
+  switch (p.r.nd) {
+    case 1: return go_small<1, 16>(p, s, sms);
+    case 2: return go_small<2, 16>(p, s, sms);
+    case 4: return go_small<4, 16>(p, s, sms);
+    case 8: return go_small<8, 16>(p, s, sms);
+    case 16: return go_small<16, 16>(p, s, sms);
+    case 32: return go_small<32, 64>(p, s, sms);
+    case 64: return go_small<64, 64>(p, s, sms);
+    default:
+      if (p.r.nd <= 64) return go_small<0, 64>(p, s, sms);
+      return cudaErrorInvalidValue;
   }
 }
 

@@ -137,7 +137,7 @@ def test_profile_calls_on_a_fresh_plan():
     with z.zero_plan_create(100, 4, 2, 8, HP) as p:
         z.zero_profile_enable(p, True)
         ms, n = z.zero_profile_read(p, reset=True)
-        assert ms == [0.0] * 4 and n == [0] * 4
+        assert ms == [0.0] * z.ZERO_PROF_KINDS and n == [0] * z.ZERO_PROF_KINDS
 
 
 def test_destroyed_plan_is_refused_by_the_binding():

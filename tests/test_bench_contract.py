@@ -60,7 +60,7 @@ def test_step_line():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 2 * 1048576
     assert e["d2h_bytes_per_step"] > 0 and set(e["by_mode"]) == {"copy", "copy_overlap",
                                                                   "zero_copy"}
-    assert d["gpu_launches"] >= 2 * 20
+    assert d["gpu_launches"] >= 20  # one launch per step for this small span, else two or three
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
