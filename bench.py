@@ -664,7 +664,8 @@ def run_ours(args, w0):
     return 0
 
 
-KERNEL_SOURCES = ("step_kernels.cu", "gather_kernel.cu", "bulk_async.h", "internal.h")
+KERNEL_SOURCES = ("step_kernels.cu", "gather_kernel.cu", "bulk_async.h", "grid_sync.h",
+                  "internal.h")
 
 
 def kernel_source_hash() -> str:

@@ -98,6 +98,7 @@ _SIGS = {
     "zero_plan_get_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
     "zero_plan_set_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
     "zero_selftest_wait": ([ctypes.c_uint32, ctypes.POINTER(_I32)], ctypes.c_int),
+    "zero_selftest_grid_barrier": ([ctypes.c_uint32, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
     "zero_last_error": ([], ctypes.c_char_p),
 }
 _lib_handle = None
@@ -457,4 +458,11 @@ def zero_selftest_wait(polls: int = 4096) -> int:
     """Run the bounded-wait self-test; 1 means the wait expired and was reported."""
     out = _I32()
     _check(_lib.zero_selftest_wait(polls, ctypes.byref(out)))
+    return out.value
+
+
+def zero_selftest_grid_barrier(polls: int = 4096, skip_one: bool = True) -> int:
+    """Run the grid-barrier self-test; 1 means the barrier gave up and reported it."""
+    out = _I32()
+    _check(_lib.zero_selftest_grid_barrier(polls, 1 if skip_one else 0, ctypes.byref(out)))
     return out.value

@@ -21,6 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 CU_SOURCES = ["step_kernels.cu", "gather_kernel.cu", "noalloc.cu", "selftest.cu"]
 CPP_SOURCES = ["plan.cpp"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "bulk_async.h"),
+           os.path.join(CSRC, "grid_sync.h"),
            os.path.join(ROOT, "include", "zero.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,10 +1,15 @@
-// Self-test of the bounded wait that every libzero kernel uses on its mbarriers.
+// Self-tests of the bounded waits of the libzero kernels.
 //
-// A one-warp kernel initialises an mbarrier that nothing will ever complete and waits on
-// it with a caller-given poll limit. The wait must give up, the kernel must record that
-// and return, and the context must stay usable. This exercises the failure path of the
-// bulk-copy kernels without faulting, trapping or hanging the GPU.
+// zero_selftest_wait: a one-warp kernel initialises an mbarrier that nothing will ever
+// complete and waits on it with a caller-given poll limit. The wait must give up, the
+// kernel must record that and return, and the context must stay usable. This exercises
+// the failure path of the bulk-copy kernels without faulting, trapping or hanging the GPU.
+//
+// zero_selftest_grid_barrier: a cooperative launch of two CTAs meets at the grid barrier
+// of the one-launch step; with skip_one set, CTA 1 leaves without arriving, so CTA 0's
+// wait must give up within its poll limit and record that.
 #include "bulk_async.h"
+#include "grid_sync.h"
 #include "internal.h"
 
 namespace zero {
@@ -21,8 +26,16 @@ __global__ void k_wait_probe(unsigned polls, int32_t* out) {
   if (threadIdx.x == 0) *out = arrived ? 0 : 1;
 }
 
+__global__ void k_barrier_probe(unsigned polls, int skip_one, unsigned* words, int32_t* out) {
+  if (threadIdx.x != 0) return;
+  if (skip_one && blockIdx.x == 1) return;  // never arrives
+  const bool met = grid_barrier(&words[0], &words[1], gridDim.x, polls);
+  if (blockIdx.x == 0) *out = met ? 0 : 1;
+}
+
 // Result word of the probe; host code gets its device address from cudaGetSymbolAddress.
 static __device__ int32_t g_probe_result;
+static __device__ unsigned g_probe_barrier[2];
 
 }  // namespace
 }  // namespace zero
@@ -40,6 +53,36 @@ extern "C" int zero_selftest_wait(uint32_t polls, int32_t* expired) {
   int32_t r = -1;
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(&r, addr, sizeof r, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error(ZERO_ECUDA, "self-test kernel failed");
+  *expired = r;
+  set_error(ZERO_OK, "");
+  return ZERO_OK;
+}
+
+extern "C" int zero_selftest_grid_barrier(uint32_t polls, int32_t skip_one, int32_t* expired) {
+  using namespace zero;
+  if (!expired) return set_error(ZERO_EINVAL, "expired is NULL");
+  if (polls < 1 || polls > (1u << 24)) return set_error(ZERO_EINVAL, "polls must be in [1, 2^24]");
+  void* res = nullptr;
+  void* words = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&res, g_probe_result);
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(&words, g_probe_barrier);
+  if (e == cudaSuccess) e = cudaMemset(res, 0xff, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(words, 0, 2 * sizeof(unsigned));
+  if (e != cudaSuccess) return set_error(ZERO_ECUDA, "self-test set-up failed");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(32);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_barrier_probe, (unsigned)polls, (int)(skip_one != 0),
+                         static_cast<unsigned*>(words), static_cast<int32_t*>(res));
+  int32_t r = -1;
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&r, res, sizeof r, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return set_error(ZERO_ECUDA, "self-test kernel failed");
   *expired = r;
   set_error(ZERO_OK, "");

@@ -28,6 +28,7 @@
 #include <math.h>
 
 #include "bulk_async.h"
+#include "grid_sync.h"
 #include "internal.h"
 
 namespace zero {
@@ -593,11 +594,6 @@ struct SmallArgs {
   long long vecs_per_cta;
 };
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned x;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
-  return x;
-}
 __device__ __forceinline__ void bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -635,30 +631,6 @@ __device__ void small_block_reduce(U128& acc, long long& bad) {
     acc = t;
     bad = b;
   }
-}
-
-// Grid-wide barrier of the cooperative launch (thread 0 of each CTA). The CTA's earlier
-// global writes are visible to every CTA once it returns true; false after
-// kBarrierPolls polls or about kWaitNs.
-__device__ bool grid_barrier(DevScratch* st, unsigned nblocks) {
-  const unsigned gen = ld_acquire_u32(&st->bar_gen);
-  __threadfence();
-  if (atomicAdd(&st->bar_count, 1u) == nblocks - 1) {
-    st->bar_count = 0;  // nobody touches the count again in this launch
-    __threadfence();
-    atomicAdd(&st->bar_gen, 1u);
-    return true;
-  }
-  const unsigned long long t0 = global_ns();
-  for (unsigned i = 0; i < kBarrierPolls; ++i) {
-    if (ld_acquire_u32(&st->bar_gen) != gen) {
-      __threadfence();
-      return true;
-    }
-    __nanosleep(64);
-    if ((i & 63u) == 63u && global_ns() - t0 > kWaitNs) return false;
-  }
-  return false;
 }
 
 template <int ND, int CAP>
@@ -735,7 +707,7 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     st->partials[blockIdx.x].lo = acc.lo;
     st->partials[blockIdx.x].hi = acc.hi;
     st->partials[blockIdx.x].bad = bad;
-    s_ok = grid_barrier(st, gridDim.x) ? 1 : 0;
+    s_ok = grid_barrier(&st->bar_count, &st->bar_gen, gridDim.x, kBarrierPolls) ? 1 : 0;
   }
   bar_sync(1, kSmallThreads);
   if (!s_ok) {

@@ -167,6 +167,7 @@ def test_scaler_and_state_calls_validate_before_touching_the_device():
 def test_selftest_rejects_bad_poll_counts():
     for polls in (0, 2**24 + 1):
         expect(z.ZERO_EINVAL, z.zero_selftest_wait, polls)
+        expect(z.ZERO_EINVAL, z.zero_selftest_grid_barrier, polls)
 
 
 def test_gather_status_without_a_gather_is_zero():

@@ -28,3 +28,19 @@ def test_context_stays_usable_after_an_expired_wait():
     r = Runner(w).run()
     assert r.exact and all(x["status"] == 0 for x in r.results)
     assert z.zero_gather_status(r.plan) == 0
+
+
+def test_grid_barrier_is_met_when_every_cta_arrives():
+    assert z.zero_selftest_grid_barrier(1 << 16, skip_one=False) == 0
+
+
+def test_grid_barrier_gives_up_when_a_cta_never_arrives():
+    for polls in (1, 64, 4096):
+        t0 = time.perf_counter()
+        assert z.zero_selftest_grid_barrier(polls, skip_one=True) == 1
+        assert time.perf_counter() - t0 < 5.0
+    # the context stays usable: a one-launch step (it uses the same barrier) afterwards
+    w = wl.Workload("after_barrier", cfg=601, n=50_001, nd=4, align=8, stage=2, r0=0, r1=4,
+                    loss_scale=1024.0, grad_sigma=1e-3, clip=1.0, steps=2)
+    r = Runner(w).run()
+    assert r.exact and all(x["status"] == 0 for x in r.results)
