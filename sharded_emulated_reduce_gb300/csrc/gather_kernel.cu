@@ -14,6 +14,8 @@
 // them into their own table): bulk loads bring the aligned 16-byte source blocks around
 // each stretch of the tile into a shared-memory ring, and all threads recombine pairs of
 // blocks (funnel shifts) into aligned 16-byte stores to global memory.
+#include <atomic>
+
 #include "bulk_async.h"
 #include "internal.h"
 
@@ -282,13 +284,18 @@ __global__ void __launch_bounds__(kMisThreads, 1)
   }
 }
 
+// Per-device values below are computed once; several host threads may race to compute
+// the same value, so they are relaxed atomics.
 int sm_count() {
-  static int sms[kMaxDevices] = {};
+  static std::atomic<int> sms[kMaxDevices];
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < kMaxDevices && sms[dev] > 0) return sms[dev];
+  if (dev >= 0 && dev < kMaxDevices) {
+    n = sms[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (dev >= 0 && dev < kMaxDevices) sms[dev] = n;
+  if (dev >= 0 && dev < kMaxDevices) sms[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -305,19 +312,19 @@ cudaError_t launch_gather(const GatherLaunch& p, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool attr_set[kMaxDevices] = {};
-  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev]) {
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGatSmem);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
+    if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   if (p.realign) {
-    static bool mis_attr_set[kMaxDevices] = {};
-    if (dev < 0 || dev >= kMaxDevices || !mis_attr_set[dev]) {
+    static std::atomic<bool> mis_attr_set[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices || !mis_attr_set[dev].load(std::memory_order_relaxed)) {
       e = cudaFuncSetAttribute(k_gather_realign, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kMisSmem);
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < kMaxDevices) mis_attr_set[dev] = true;
+      if (dev >= 0 && dev < kMaxDevices) mis_attr_set[dev].store(true, std::memory_order_relaxed);
     }
     const int grid = p.grid > 0 ? p.grid : gather_grid(p.tiles);
     k_gather_realign<<<grid, kMisThreads, kMisSmem, s>>>(p);

@@ -27,6 +27,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "bulk_async.h"
 #include "grid_sync.h"
 #include "internal.h"
@@ -833,36 +835,39 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
 
 constexpr int kMaxDevices = 64;
 
+// Per-device values below are computed once; several host threads may race to compute
+// the same value, so they are relaxed atomics.
+
 // SM count of the current device, looked up once per device.
 int sm_count(int* dev_out) {
-  static int sms[kMaxDevices] = {};
+  static std::atomic<int> sms[kMaxDevices];
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev_out) *dev_out = dev;
-  if (dev < 0 || dev >= kMaxDevices) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n;
+  int n = 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    n = sms[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
   }
-  if (sms[dev] == 0) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev];
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < kMaxDevices) sms[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // Persistent grid for `kernel`: SMs x resident CTAs per SM, capped by the CTAs the work
 // needs. `per_sm` is the caller's per-device cache for this kernel (one static table per
 // launcher instantiation, because kernels of the same signature differ in occupancy).
 template <typename K>
-int occupancy_grid(K kernel, long long work_items, int (&per_sm)[kMaxDevices],
+int occupancy_grid(K kernel, long long work_items, std::atomic<int> (&per_sm)[kMaxDevices],
                    int* resident = nullptr) {
   int dev = 0;
   const int sms = sm_count(&dev);
   int occ = 0;
-  if (dev >= 0 && dev < kMaxDevices && per_sm[dev] > 0) {
-    occ = per_sm[dev];
-  } else {
+  if (dev >= 0 && dev < kMaxDevices) occ = per_sm[dev].load(std::memory_order_relaxed);
+  if (occ <= 0) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
     if (occ < 1) occ = 1;
-    if (dev >= 0 && dev < kMaxDevices) per_sm[dev] = occ;
+    if (dev >= 0 && dev < kMaxDevices) per_sm[dev].store(occ, std::memory_order_relaxed);
   }
   long long g = (long long)sms * occ;
   if (resident) *resident = (int)(g < 0x7fffffff ? g : 0x7fffffff);
@@ -885,7 +890,7 @@ cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
   a.hp = p.hp;
   a.nd = p.nd;
   a.finalize = p.finalize ? 1 : 0;
-  static int occ_cache[kMaxDevices] = {};  // this instantiation's occupancy per device
+  static std::atomic<int> occ_cache[kMaxDevices];  // this instantiation's occupancy
   // One wave of reducing CTAs. When the span needs less than a wave, a spare CTA slot
   // computes the next step's t-only scalars, which takes their double-precision powers
   // off the serial combine; a full wave keeps every slot for the reduce (one CTA fewer
@@ -924,13 +929,15 @@ namespace {
 // The fused kernel's shared-memory limit, raised once per instantiation and device.
 template <int ND, int CAP>
 cudaError_t prepare_small() {
-  static bool done[kMaxDevices] = {};
+  static std::atomic<bool> done[kMaxDevices];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < kMaxDevices && done[dev]) return cudaSuccess;
+  if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_relaxed))
+    return cudaSuccess;
   const cudaError_t e = cudaFuncSetAttribute(
       k_step_small<ND, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSmem);
-  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices)
+    done[dev].store(true, std::memory_order_relaxed);
   return e;
 }
 
@@ -970,10 +977,13 @@ cudaError_t go_small(const SmallLaunch& p, cudaStream_t s, int sms) {
 }  // namespace
 
 long long small_step_max_vecs() {
-  static long long cache[kMaxDevices] = {};
+  static std::atomic<long long> cache[kMaxDevices];
   int dev = 0;
   const int sms = sm_count(&dev);
-  if (dev >= 0 && dev < kMaxDevices && cache[dev] != 0) return cache[dev] > 0 ? cache[dev] : 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const long long c = cache[dev].load(std::memory_order_relaxed);
+    if (c != 0) return c > 0 ? c : 0;
+  }
   // every instantiation must fit one CTA per SM; the generic one holds the most registers
   int occ = 0, occ8 = 0;
   cudaError_t e = prepare_small<0, 64>();
@@ -985,7 +995,7 @@ long long small_step_max_vecs() {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ8, k_step_small<8, 16>,
                                                       kSmallThreads + 32, kSmallSmem);
   const long long v = (e == cudaSuccess && occ >= 1 && occ8 >= 1) ? (long long)sms * kSmallVecs : -1;
-  if (dev >= 0 && dev < kMaxDevices) cache[dev] = v;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
   return v > 0 ? v : 0;
 }
 
@@ -1027,12 +1037,12 @@ cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s) {
   a.st = p.scratch;
   int dev = 0;
   const int sms = sm_count(&dev);
-  static bool attr_set[kMaxDevices] = {};
-  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev]) {
+  static std::atomic<bool> attr_set[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_relaxed)) {
     cudaError_t e = cudaFuncSetAttribute(k_update, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kUpdSmem);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
+    if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   const long long tiles = ((p.n_valid & ~7ll) + kUpdTile - 1) / kUpdTile;
   long long grid = tiles < sms ? tiles : sms;  // one CTA per SM, persistent

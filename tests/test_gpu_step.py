@@ -339,3 +339,44 @@ def test_two_plans_on_two_streams_concurrently():
         for a, b in zip(got, alone[k]):
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
         plans[k].close()
+
+
+@pytest.mark.parametrize("n", [400_003, 3_000_001])
+def test_two_host_threads_each_with_a_plan(n):
+    # one plan per host thread, stepping at the same time (the library's host code runs
+    # concurrently: ctypes releases the interpreter lock); each thread's state must be the
+    # bits of the same steps run alone. 400,003 parameters take the one-launch step,
+    # 3,000,001 the two-kernel step with the second stream.
+    import threading
+    ws_ = [small(n=n, nd=4, cfg=270 + k, steps=3) for k in range(2)]
+    grads = [[wl.make_grads(w, s) for s in range(w.steps)] for w in ws_]
+
+    def run(k, out):
+        w = ws_[k]
+        st = wl.make_state(w)
+        p = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+        z.zero_plan_bind(p, 0, w.nd, *st, 0)
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            for s in range(w.steps):
+                z.zero_shard_step(p, 0, w.nd, grads[k][s], w.loss_scale, w.clip, stream)
+            out[k] = z.zero_step_result(p).as_dict()
+        out[k]["state"] = [f32(t).copy() if t.dtype == torch.float32 else h16(t).copy()
+                           for t in st[:4]]
+        p.close()
+
+    alone = {}
+    for k in range(2):
+        run(k, alone)
+    torch.cuda.synchronize()
+    together = {}
+    threads = [threading.Thread(target=run, args=(k, together)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    for k in range(2):
+        assert together[k]["step"] == alone[k]["step"] == 3
+        for a, b in zip(together[k]["state"], alone[k]["state"]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
