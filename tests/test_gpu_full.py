@@ -4,7 +4,8 @@ The oracle streams every gradient of every step through its rank-order reduce an
 sum of squares (so the norm, clip coefficient, overflow flag and skip decision are
 checked exactly), and follows a sample of elements (random ones plus the span ends and
 shard boundaries) through every step. The ZeRO-3 gather is checked on sampled elements
-against the oracle and in full against slices of the shards.
+against the oracle and in full against slices of the shards, for the workload's layer
+boundaries and for boundaries moved off the shards' 16-byte alignment.
 """
 import numpy as np
 import pytest
@@ -75,4 +76,31 @@ def test_zero3_13b_rank0_nd64_step_and_gather():
         got = h16(dst[l][torch.as_tensor(js, device="cuda")])
         for j, g in zip(js.tolist(), got.tolist()):
             rank, off = oracle.gather_source(s, offs[l] + j)
+            assert g == int(h16(shards[rank][off:off + 1])[0])
+    # the same shards with every interior layer boundary moved by 3 elements (the bench's
+    # --layer-shift 3): layers 1..39 are misaligned against the shards modulo 16 bytes and
+    # go through the realigning kernel
+    del dst
+    torch.cuda.empty_cache()
+    offs3 = [offs[0]] + [o + 3 for o in offs[1:-1]] + [offs[-1]]
+    dst3 = [torch.empty(offs3[l + 1] - offs3[l], dtype=torch.float16, device="cuda")
+            for l in range(len(offs3) - 1)]
+    z.zero_gather_layers(r.plan, offs3, shards, dst3)
+    torch.cuda.synchronize()
+    assert z.zero_gather_status(r.plan) == 0
+    for l in range(len(offs3) - 1):
+        a, b = offs3[l], offs3[l + 1]
+        rr = a // s
+        pos = a
+        while pos < b:
+            hi = min(b, (rr + 1) * s)
+            assert torch.equal(dst3[l][pos - a:hi - a], shards[rr][pos - rr * s:hi - rr * s]), l
+            pos = hi
+            rr += 1
+    for l in [0, 1, 20, 39]:
+        n_l = offs3[l + 1] - offs3[l]
+        js = np.unique(np.concatenate([rng.integers(0, n_l, 512), [0, 1, 2, n_l - 1]]))
+        got = h16(dst3[l][torch.as_tensor(js, device="cuda")])
+        for j, g in zip(js.tolist(), got.tolist()):
+            rank, off = oracle.gather_source(s, offs3[l] + j)
             assert g == int(h16(shards[rank][off:off + 1])[0])
