@@ -27,6 +27,18 @@ def test_gpt2_small_flat_nd8_all_steps():
     assert all(x["skipped"] == 0 for x in r.results)
     assert all(x["clip_coef"] < 1.0 for x in r.results)  # clipping is active here
     assert r.exact
+    # the ZeRO-1/2 parameter all-gather after the step: the Nd fp16 shards (rank 0's is the
+    # step's output, the others seeded) into one flat buffer, as the bench's full-buffer
+    # gather times it; the padding of the last shard is not copied
+    _, s = w.layout()
+    shards = wl.make_shards(w, r.state[3][:s])
+    flat = torch.empty(w.n, dtype=torch.float16, device="cuda")
+    z.zero_gather_layers(r.plan, [0, w.n], shards, [flat])
+    torch.cuda.synchronize()
+    assert z.zero_gather_status(r.plan) == 0
+    for k in range(w.nd):
+        hi = min(w.n, (k + 1) * s)
+        assert torch.equal(flat[k * s:hi], shards[k][:hi - k * s]), k
 
 
 def test_flat_1p3b_nd16_overflow_skip():
