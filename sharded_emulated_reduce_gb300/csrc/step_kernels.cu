@@ -117,11 +117,24 @@ __device__ __noinline__ DevPre pre_scalars_call(long long t, const HostHParams& 
   return pre_scalars(t, hp);
 }
 
-// Whether slot `p` holds the t-only scalars of step counter t under hp (read through L2).
-__device__ __forceinline__ bool pre_matches(const DevPre* p, long long t, const HostHParams& hp) {
-  return __ldcg(&p->valid) == kPreValid && __ldcg(&p->t) == t && __ldcg(&p->lr) == hp.lr &&
-         __ldcg(&p->beta1) == hp.beta1 &&
-         __ldcg(&p->beta2) == hp.beta2 && __ldcg(&p->weight_decay) == hp.weight_decay;
+static_assert(sizeof(DevPre) == 48, "a slot is three 16-byte vectors");
+
+// Slot `p` read through L2 in one round trip (three independent 16-byte loads).
+__device__ __forceinline__ DevPre load_pre(const DevPre* p) {
+  const int4* q = reinterpret_cast<const int4*>(p);
+  const int4 w0 = __ldcg(q), w1 = __ldcg(q + 1), w2 = __ldcg(q + 2);
+  DevPre r;
+  int4* o = reinterpret_cast<int4*>(&r);
+  o[0] = w0;
+  o[1] = w1;
+  o[2] = w2;
+  return r;
+}
+
+// Whether a slot holds the t-only scalars of step counter t under hp.
+__device__ __forceinline__ bool pre_matches(const DevPre& p, long long t, const HostHParams& hp) {
+  return p.valid == kPreValid && p.t == t && p.lr == hp.lr && p.beta1 == hp.beta1 &&
+         p.beta2 == hp.beta2 && p.weight_decay == hp.weight_decay;
 }
 
 // The t-only scalars for step counter t: from slot t & 1 when its tag matches, otherwise
@@ -130,14 +143,9 @@ __device__ __forceinline__ bool pre_matches(const DevPre* p, long long t, const 
 template <bool INLINE>
 __device__ __forceinline__ DevPre t_scalars(const DevScratch* st, long long t,
                                             const HostHParams& hp) {
-  DevPre pre;
-  const DevPre* slot = &st->pre[t & 1];
-  if (pre_matches(slot, t, hp)) {
-    pre.omb1 = __ldcg(&slot->omb1);
-    pre.omb2 = __ldcg(&slot->omb2);
-    pre.bc1 = __ldcg(&slot->bc1);
-    pre.bc2 = __ldcg(&slot->bc2);
-    pre.decay = __ldcg(&slot->decay);
+  DevPre pre = load_pre(&st->pre[t & 1]);
+  if (pre_matches(pre, t, hp)) {
+    // the slot's values
   } else if constexpr (INLINE) {
     pre = pre_scalars(t, hp);
   } else {
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, (ND >= 32) ? 5 : 0)
       if (threadIdx.x == 0) {
         const long long tn = st->step + 1;
         DevPre* slot = &st->pre[tn & 1];
-        if (!pre_matches(slot, tn, a.hp)) *slot = pre_scalars_call(tn, a.hp);
+        if (!pre_matches(load_pre(slot), tn, a.hp)) *slot = pre_scalars_call(tn, a.hp);
       }
       return;
     }
@@ -400,7 +408,7 @@ __global__ void k_next_scalars(DevScratch* st, HostHParams hp) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   const long long t = st->step;
   DevPre* slot = &st->pre[t & 1];
-  if (!pre_matches(slot, t, hp)) *slot = pre_scalars_call(t, hp);
+  if (!pre_matches(load_pre(slot), t, hp)) *slot = pre_scalars_call(t, hp);
 }
 
 struct UpdateArgs {
@@ -656,7 +664,7 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
       bar_arrive(2, 64);                  // CTA 0's commit waits for this read
       if (tid == kSmallThreads) {
         DevPre* slot = &st->pre[tn & 1];
-        if (!pre_matches(slot, tn, a.r.hp)) *slot = pre_scalars_call(tn, a.r.hp);
+        if (!pre_matches(load_pre(slot), tn, a.r.hp)) *slot = pre_scalars_call(tn, a.r.hp);
       }
     }
     return;
@@ -689,9 +697,7 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   // 1. rank-order sums of this CTA's slice into shared memory, and its statistics
   U128 acc{0, 0};
   long long bad = 0;
-  for (long long v = v0 + tid; v < v1; v += kSmallThreads) {
-    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    sum_group<ND, CAP>(a.r, v, s);
+  auto finish = [&](long long v, float (&s)[8]) {  // statistics, then the sums to smem
     const long long base = v * 8;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -703,6 +709,11 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     float4* o = reinterpret_cast<float4*>(sums) + 2 * (v - v0);
     o[0] = make_float4(s[0], s[1], s[2], s[3]);
     o[1] = make_float4(s[4], s[5], s[6], s[7]);
+  };
+  for (long long v = v0 + tid; v < v1; v += kSmallThreads) {
+    float s0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    sum_group<ND, CAP>(a.r, v, s0);
+    finish(v, s0);
   }
   small_block_reduce(acc, bad);
   if (tid == 0) {
