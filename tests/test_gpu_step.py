@@ -380,3 +380,21 @@ def test_two_host_threads_each_with_a_plan(n):
         assert together[k]["step"] == alone[k]["step"] == 3
         for a, b in zip(together[k]["state"], alone[k]["state"]):
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_one_launch_step_boundary():
+    # the largest span the one-launch step takes (1024 groups of 8 per SM) and the
+    # smallest one past it, which runs the reduce and update kernels; both follow the oracle
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_max = sms * 1024 * 8
+    for n, one_launch in ((n_max, True), (n_max + 8, False)):
+        w = small(n=n, nd=4, cfg=280 + int(one_launch), steps=2)
+        r = Runner(w).run()
+        assert r.exact
+        ms, counts = z.zero_profile_read(r.plan)
+        z.zero_profile_enable(r.plan, True)
+        grads = wl.make_grads(w, 0)
+        z.zero_shard_step(r.plan, 0, 4, grads, w.loss_scale, w.clip)
+        ms, counts = z.zero_profile_read(r.plan, reset=True)
+        assert (counts[z.PROF_STEP] == 1) == one_launch, (n, counts)
+        r.plan.close()
