@@ -427,7 +427,9 @@ def run_ours(args, w0):
 
     master, m, v, p16, ws = wl.make_state(w, dev)
     if args.state == "host":
-        master, m, v, p16 = [t.cpu().pin_memory() for t in (master, m, v, p16)]
+        # optimizer state in Grace memory; the fp16 parameters stay in HBM, where the
+        # forward pass reads them
+        master, m, v = [t.cpu().pin_memory() for t in (master, m, v)]
     gsets = [wl.make_grads(w, s, dev) for s in range(1 if args.one_set else 2)]
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
     z.zero_plan_bind(plan, w.r0, w.r1, master, m, v, p16, ws, 0)
@@ -638,7 +640,8 @@ def run_ours(args, w0):
     if graphs is not None:
         cfg["launch"] = "CUDA graph replay (one graph per gradient set)"
     if args.state == "host":
-        cfg["state"] = "pinned Grace memory over NVLink-C2C (master/m/v/param16)"
+        cfg["state"] = ("master/m/v in pinned Grace memory over NVLink-C2C; fp16 parameters "
+                        "in HBM")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -803,8 +806,8 @@ def main(argv=None):
                     help="CPU oracle baseline budget (0 skips it)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
     ap.add_argument("--state", default="device", choices=["device", "host"],
-                    help="where master/m/v/param16 live: HBM, or pinned Grace memory read "
-                         "and written over NVLink-C2C")
+                    help="where master/m/v live: HBM, or pinned Grace memory read and "
+                         "written over NVLink-C2C (the fp16 parameters stay in HBM)")
     ap.add_argument("--prefetch", action="store_true",
                     help="gather: one launch and one event per layer (zero_prefetch_layers)")
     ap.add_argument("--layer-shift", type=int, default=0,
