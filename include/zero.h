@@ -161,7 +161,7 @@ int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float
  * span's real parameters, and, unless the flag is set, the AdamW update of master,
  * exp_avg and exp_avg_sq with the fp16 cast into param16; the step counter advances
  * only on an applied step. Enqueued on stream; no host synchronisation. A span of at
- * most 1024 groups of 8 parameters per SM (and nd <= 64) runs as one cooperative launch
+ * most 3072 groups of 8 parameters per SM (and nd <= 64) runs as one cooperative launch
  * that keeps the fp32 sums in shared memory; other spans run a reduce and an update
  * kernel. When the span
  * fills at least one wave of the reduce, a one-thread kernel computing the next step's

@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
 }
 
 // ---- the fused step for small spans -------------------------------------------------
-// A span of at most kSmallVecs groups of 8 per SM runs as one cooperative launch (all
+// A span of at most kWideVecs groups of 8 per SM runs as one cooperative launch (all
 // CTAs resident at once), one 512-thread CTA per SM, each owning a contiguous slice:
 //   1. the CTA sums its slice of the contributions in rank order into shared memory and
 //      publishes its 128-bit sum of squares and non-finite count;
@@ -584,16 +584,22 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
 //      integers in the same order, so every CTA derives the same scalars; CTA 0 commits
 //      them (and the step counter and scaler) to the scratch;
 //   3. unless the step is skipped, the CTA updates its slice from the sums it kept.
-// The fp32 sums never go to HBM and the step is one launch. The CTA's master/m/v slice
-// is brought into shared memory by bulk loads issued at the start, so it arrives while
-// the CTA reduces and waits at the barrier. A 17th warp of CTA 0
+// The fp32 sums never go to HBM and the step is one launch. A slice of at most
+// kSmallVecs groups also has its master/m/v brought into shared memory by bulk loads
+// issued at the start, so they arrive while the CTA reduces and waits at the barrier;
+// a longer slice reads them from global memory in the update. A 17th warp of CTA 0
 // prepares the next step's t-only scalars meanwhile; it reads the step counter before
 // CTA 0 may advance it (named barrier 2), and the CTAs' own synchronisation uses named
 // barrier 1 over the 512 working threads only.
 constexpr int kSmallThreads = 512;
-constexpr int kSmallVecs = 1024;  // groups of 8 per CTA: 32 KiB of fp32 sums
+constexpr int kSmallVecs = 1024;  // groups of 8 per CTA whose state is prefetched
+constexpr int kWideVecs = 3072;   // groups of 8 per CTA at most (96 KiB of fp32 sums)
 constexpr size_t kSmallSlice = (size_t)kSmallVecs * 8 * sizeof(float);  // one fp32 array
-constexpr size_t kSmallSmem = 4 * kSmallSlice + 16;  // sums, master, m, v, mbarrier
+// shared memory: sums, master, m, v (kSmallSlice each) and an mbarrier; a slice longer
+// than kSmallVecs groups keeps only its sums there (up to kWideVecs groups) and reads
+// its state from global memory in the update
+constexpr size_t kSmallSmem = 4 * kSmallSlice + 16;
+static_assert((size_t)kWideVecs * 8 * sizeof(float) <= 4 * kSmallSlice, "sums fit");
 constexpr unsigned kBarrierPolls = 1u << 24;
 
 template <int CAP>
@@ -677,7 +683,9 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   long long e1 = v1 * 8;
   if (e1 > a.r.n_valid) e1 = a.r.n_valid;
   const long long eq = e1 > e0 ? e0 + (((e1 - e0) >> 2) << 2) : e0;
-  const uint32_t state_bytes = (uint32_t)((eq - e0) * sizeof(float));  // 16-byte multiple
+  const bool prefetch = a.vecs_per_cta <= kSmallVecs;  // the same for every CTA
+  const uint32_t state_bytes =
+      prefetch ? (uint32_t)((eq - e0) * sizeof(float)) : 0u;  // 16-byte multiple
   if (tid == 0) {
     s_t = st->step;  // before this CTA arrives at the barrier, so before any commit
     s_scaler = st->scaler;
@@ -816,21 +824,36 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   float* __restrict__ vv = a.v;
   const long long nq = (eq - e0) >> 2;  // whole quads of parameters
   const float4* g4 = reinterpret_cast<const float4*>(sums);
-  for (long long q = tid; q < nq; q += kSmallThreads) {
-    const long long i = e0 + 4 * q;
-    const float4 g = g4[q];
-    const float4 p = reinterpret_cast<const float4*>(s_master)[q];
-    float4 m = reinterpret_cast<const float4*>(s_m)[q];
-    float4 v = reinterpret_cast<const float4*>(s_v)[q];
-    float4 r;
-    r.x = adam_elem(g.x, p.x, m.x, v.x, c);
-    r.y = adam_elem(g.y, p.y, m.y, v.y, c);
-    r.z = adam_elem(g.z, p.z, m.z, v.z, c);
-    r.w = adam_elem(g.w, p.w, m.w, v.w, c);
-    *reinterpret_cast<float4*>(master + i) = r;
-    *reinterpret_cast<float4*>(mm + i) = m;
-    *reinterpret_cast<float4*>(vv + i) = v;
-    *reinterpret_cast<uint2*>(a.p16 + i) = make_uint2(pack_h2(r.x, r.y), pack_h2(r.z, r.w));
+  // one loop per state source (shared memory or global), so the loop itself has no branch
+  auto update = [&](auto load_state) {
+    for (long long q = tid; q < nq; q += kSmallThreads) {
+      const long long i = e0 + 4 * q;
+      const float4 g = g4[q];
+      float4 p, m, v;
+      load_state(q, i, p, m, v);
+      float4 r;
+      r.x = adam_elem(g.x, p.x, m.x, v.x, c);
+      r.y = adam_elem(g.y, p.y, m.y, v.y, c);
+      r.z = adam_elem(g.z, p.z, m.z, v.z, c);
+      r.w = adam_elem(g.w, p.w, m.w, v.w, c);
+      *reinterpret_cast<float4*>(master + i) = r;
+      *reinterpret_cast<float4*>(mm + i) = m;
+      *reinterpret_cast<float4*>(vv + i) = v;
+      *reinterpret_cast<uint2*>(a.p16 + i) = make_uint2(pack_h2(r.x, r.y), pack_h2(r.z, r.w));
+    }
+  };
+  if (prefetch) {
+    update([&](long long q, long long, float4& p, float4& m, float4& v) {
+      p = reinterpret_cast<const float4*>(s_master)[q];
+      m = reinterpret_cast<const float4*>(s_m)[q];
+      v = reinterpret_cast<const float4*>(s_v)[q];
+    });
+  } else {
+    update([&](long long, long long i, float4& p, float4& m, float4& v) {
+      p = *reinterpret_cast<const float4*>(master + i);
+      m = *reinterpret_cast<const float4*>(mm + i);
+      v = *reinterpret_cast<const float4*>(vv + i);
+    });
   }
   if (tid < e1 - eq) {  // at most 3 parameters, at the end of the real ones
     const long long i = eq + tid;
@@ -1005,7 +1028,7 @@ long long small_step_max_vecs() {
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ8, k_step_small<8, 16>,
                                                       kSmallThreads + 32, kSmallSmem);
-  const long long v = (e == cudaSuccess && occ >= 1 && occ8 >= 1) ? (long long)sms * kSmallVecs : -1;
+  const long long v = (e == cudaSuccess && occ >= 1 && occ8 >= 1) ? (long long)sms * kWideVecs : -1;
   if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
   return v > 0 ? v : 0;
 }

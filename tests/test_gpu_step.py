@@ -164,7 +164,7 @@ def test_profile_counts_every_launch():
 def test_profile_counts_the_next_step_scalars_of_a_full_wave_span():
     # a span that fills the reduce's wave computes the next step's scalars in a one-thread
     # kernel on the plan's second stream: one more launch of kind 2 per step
-    w = small(n=3_000_000, nd=4, cfg=211, steps=1)
+    w = small(n=5_000_000, nd=4, cfg=211, steps=1)
     master, m, v, p16, ws = wl.make_state(w)
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
     z.zero_plan_bind(plan, 0, 4, master, m, v, p16, ws, 0)
@@ -261,13 +261,13 @@ def test_dist_step_in_one_process_group_equals_step():
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("n", [300_001, 3_000_001])
+@pytest.mark.parametrize("n", [300_001, 6_000_001])
 def test_step_captured_in_a_cuda_graph_matches_eager_steps(n):
     # the step's launches make no host-side decision, so they can be captured once and
     # replayed; replays must give the same bits as eager calls (including an overflow
-    # skip). 300,001 parameters need less than one wave of the reduce (its spare CTA
-    # computes the next step's scalars); 3,000,001 fill it, and the capture then holds
-    # the fork to the plan's second stream, its one-thread kernel and the join.
+    # skip). 300,001 parameters take the one-launch step (a cooperative kernel node);
+    # 6,000,001 run the reduce and update kernels with a full wave, and the capture then
+    # holds the fork to the plan's second stream, its one-thread kernel and the join.
     w = small(n=n, nd=8, r1=8, cfg=250, steps=4, inject=((2, 3, wl.POS_INF, 4321),))
     first, n_span, n_valid = w.span()
     results = []
@@ -341,12 +341,12 @@ def test_two_plans_on_two_streams_concurrently():
         plans[k].close()
 
 
-@pytest.mark.parametrize("n", [400_003, 3_000_001])
+@pytest.mark.parametrize("n", [400_003, 5_000_001])
 def test_two_host_threads_each_with_a_plan(n):
     # one plan per host thread, stepping at the same time (the library's host code runs
     # concurrently: ctypes releases the interpreter lock); each thread's state must be the
     # bits of the same steps run alone. 400,003 parameters take the one-launch step,
-    # 3,000,001 the two-kernel step with the second stream.
+    # 5,000,001 the two-kernel step with the second stream.
     import threading
     ws_ = [small(n=n, nd=4, cfg=270 + k, steps=3) for k in range(2)]
     grads = [[wl.make_grads(w, s) for s in range(w.steps)] for w in ws_]
@@ -383,11 +383,12 @@ def test_two_host_threads_each_with_a_plan(n):
 
 
 def test_one_launch_step_boundary():
-    # the largest span the one-launch step takes (1024 groups of 8 per SM) and the
-    # smallest one past it, which runs the reduce and update kernels; both follow the oracle
+    # the one-launch step bulk-loads the state of slices up to 1024 groups of 8 per SM
+    # and reads it from global memory up to 3072; the smallest span past that runs the
+    # reduce and update kernels; all follow the oracle
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    n_max = sms * 1024 * 8
-    for n, one_launch in ((n_max, True), (n_max + 8, False)):
+    n_pre, n_max = sms * 1024 * 8, sms * 3072 * 8
+    for n, one_launch in ((n_pre, True), (n_pre + 8, True), (n_max, True), (n_max + 8, False)):
         w = small(n=n, nd=4, cfg=280 + int(one_launch), steps=2)
         r = Runner(w).run()
         assert r.exact
