@@ -248,12 +248,13 @@ int zero_memory_bytes(int64_t n_params, int32_t nd, int32_t align, int32_t stage
 int zero_profile_enable(zero_plan* plan, int32_t on);
 int zero_profile_read(zero_plan* plan, double* ms, int64_t* launches, int32_t reset);
 
-/* A shard step that allocates nothing. The paper has no counterpart: this is an interface
+/* A shard step that allocates nothing. The pages have no counterpart: this is an interface
  * variant of zero_shard_step for callers that cannot allocate device memory when they step
  * (a framework that reserved all of HBM for its own pool at start-up and forbids later
  * cudaMalloc calls, an allocator hook that must not re-enter its allocator, or a loop in
  * which the device-wide synchronisation that cudaMalloc/cudaFree may cause is not
- * acceptable). It needs no plan and runs the same reduce and update kernels.
+ * acceptable). It needs no plan and runs the same kernels as zero_shard_step (one
+ * cooperative launch for a small span, else the reduce and update kernels).
  *   nd: ranks, 1..ZERO_MAX_ND; n: span length, a multiple of 8, 8 <= n <=
  *     ZERO_NOALLOC_MAX_SPAN; n_valid: real parameters at the start of the span (0..n);
  *     n * nd^2 < 2^47;
@@ -267,7 +268,7 @@ int zero_profile_read(zero_plan* plan, double* ms, int64_t* launches, int32_t re
  * (16.03 MiB), which every GPU that loads the library holds until the process exits. The
  * first call on a device looks up that array's device address (cudaGetSymbolAddress) and
  * caches it; make that first call before any stream capture. Every call shares the array
- * and it keeps the last call's contents (the control word that must start at zero is
+ * and it keeps the last call's contents (the control words that must start at zero are
  * cleared by each call), so calls whose work overlaps on the GPU race and give wrong
  * results: order them on one stream or with events. Enqueued on stream; asynchronous.
  * Errors: ZERO_EINVAL (including n > ZERO_NOALLOC_MAX_SPAN), ZERO_EALIGN, ZERO_ECUDA;

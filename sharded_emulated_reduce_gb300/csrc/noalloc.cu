@@ -15,6 +15,8 @@
 // race on it and produce wrong results.
 #include <mutex>
 
+#include <cstddef>
+
 #include "internal.h"
 
 namespace zero {
@@ -100,12 +102,39 @@ extern "C" int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid,
   float* gsum = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kCtrlBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // The ticket of the last-arriving CTA must start at zero; the step counter is the
-  // caller's and is copied in and out around the two kernels.
-  e = cudaMemsetAsync(&st->ticket, 0, sizeof st->ticket, s);
+  // The ticket of the last-arriving CTA and the grid barrier's words (which follow it)
+  // must start at zero; the step counter is the caller's and is copied in and out
+  // around the kernels.
+  static_assert(offsetof(DevScratch, bar_gen) - offsetof(DevScratch, ticket) ==
+                    3 * sizeof(unsigned), "ticket, gather status, barrier words are adjacent");
+  e = cudaMemsetAsync(&st->ticket, 0, 4 * sizeof(unsigned), s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(&st->step, step_counter, sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return bad(ZERO_ECUDA, "scratch set-up copy failed");
+
+  const HostHParams hpp = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+  if (nd <= 64 && n / 8 <= small_step_max_vecs()) {  // the whole step in one launch
+    SmallLaunch sl{};
+    sl.r.grads = grad_ptrs;
+    sl.r.nd = nd;
+    sl.r.gsum = nullptr;
+    sl.r.n_span = n;
+    sl.r.n_valid = n_valid;
+    sl.r.scratch = st;
+    sl.r.finalize = true;
+    sl.r.loss_scale = loss_scale;
+    sl.r.clip = clip;
+    sl.r.hp = hpp;
+    sl.master = master;
+    sl.exp_avg = exp_avg;
+    sl.exp_avg_sq = exp_avg_sq;
+    sl.param16 = param16;
+    e = launch_small_step(sl, s);
+    if (e != cudaSuccess) return bad(ZERO_ECUDA, "fused step launch failed");
+    e = cudaMemcpyAsync(step_counter, &st->step, sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return bad(ZERO_ECUDA, "step counter copy failed");
+    return ZERO_OK;
+  }
 
   ReduceLaunch rl{};
   rl.grads = grad_ptrs;
@@ -117,7 +146,7 @@ extern "C" int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid,
   rl.finalize = true;
   rl.loss_scale = loss_scale;
   rl.clip = clip;
-  rl.hp = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+  rl.hp = hpp;
   rl.grid = 0;
   e = launch_reduce(rl, s);
   if (e != cudaSuccess) return bad(ZERO_ECUDA, "reduce launch failed");

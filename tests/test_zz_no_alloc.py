@@ -22,8 +22,11 @@ from parity import assert_p16_close, assert_state_close, f32, h16
 pytestmark = pytest.mark.gpu
 
 
-def test_noalloc_step_matches_plan_step_on_two_calls():
-    w = wl.Workload("noalloc", cfg=300, n=3_000_001, nd=8, align=8, stage=2, r0=0, r1=8,
+@pytest.mark.parametrize("n", [3_000_001, 4_194_304])
+def test_noalloc_step_matches_plan_step_on_two_calls(n):
+    # 3,000,001 parameters take the one-launch step; the largest span the array holds
+    # (4,194,304) runs the reduce and update kernels
+    w = wl.Workload("noalloc", cfg=300, n=n, nd=8, align=8, stage=2, r0=0, r1=8,
                     loss_scale=65536.0, grad_sigma=1e-3, clip=1.0, steps=2, m_sigma=1e-3,
                     v_sigma=1e-6)
     first, n_span, n_valid = w.span()
