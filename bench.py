@@ -1,19 +1,22 @@
 """Benchmark of the ZeRO shard step on GB300: parameters updated per second and achieved
-HBM bandwidth against the measured peak.
+HBM bandwidth against the measured peak, with the parameter gather after it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one pass of the whole hot path over one batch of synthetic input: the
-rank-order sum of the Nd fp16 gradient contributions, the overflow flag and exact norm,
-and the clipped AdamW update with the fp16 cast (two kernels). The default workload is
-the GPT-2-small-sized flat buffer (N = 124,439,808, Nd = 8, 128-element alignment, clip
-1.0). Inputs (2 GB of gradients per step, two alternating sets) are larger than L2, so no
-flush is needed between steps.
+A step is one pass of the shard step over one batch of synthetic input: the rank-order
+sum of the Nd fp16 gradient contributions, the overflow flag and exact norm, and the
+clipped AdamW update with the fp16 cast. The default workload is the largest one that
+fits one GPU: rank 0 of a 13B-parameter, 40-layer ZeRO-3 group of Nd = 64 (a span of
+203,125,000 parameters with 64 fp16 contributions, 26 GB per step; two alternating
+gradient sets, larger than L2, so no flush), followed in the same line by the gather of
+all 64 fp16 shards (rank 0's is the step's output) into the 40 layer buffers, and by a
+pass of both together.
 
-For N > 1 (launched with torch.distributed.run, one process per GPU) GPU g owns the
-logical ranks [g*Nd/N, (g+1)*Nd/N) of the same model (strong scaling); the one exchange
-step is an NCCL all-reduce of the 64-byte statistics buffer between the two halves of
-the step.
+For N > 1 (launched with torch.distributed.run, one process per GPU): a workload whose
+span is one logical rank gives GPU g the shard of logical rank g (weak scaling); one
+whose span covers several logical ranks splits them over the GPUs (strong scaling). The
+one exchange step is an NCCL all-reduce of the 64-byte statistics buffer between the two
+halves of the step.
 
 ``--impl reference`` times the CPU oracle (its C steps partitioned over the host cores) on
 a bounded sample of the same workload instead; it needs no GPU.
@@ -68,7 +71,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
-        self.t0 = self.t1 = None
+        self.windows = []  # (start, end) of each GPU-timed region
 
     def start(self):
         try:
@@ -87,10 +90,13 @@ class ClockSampler:
             self.lines.append((time.time(), line.strip()))
 
     def mark(self, which):
+        """Open ("start") or close ("end") a timed window; clocks are summarised over the
+        samples taken inside any window (host-bound legs, where the GPU idles, are left
+        out)."""
         if which == "start":
-            self.t0 = time.time()
-        else:
-            self.t1 = time.time()
+            self.windows.append([time.time(), None])
+        elif self.windows:
+            self.windows[-1][1] = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -107,7 +113,8 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             rows.append((ts, parts))
-        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e18)]
+        inside = [r for r in rows
+                  if any(a <= r[0] <= (b or 1e18) for a, b in self.windows)]
         used = inside or rows[-3:]
         sm = [float(p[1]) for _, p in used if p[1].replace(".", "").isdigit()]
         smax = [float(p[2]) for _, p in used if p[2].replace(".", "").isdigit()]
@@ -213,7 +220,9 @@ class PartitionedOracle:
         self.slices = [slice(cuts[i], cuts[i + 1]) for i in range(self.threads)]
         self.pool = ThreadPoolExecutor(self.threads)
 
-    def step(self, grads, master, m, v, p16, loss_scale, clip, hp, t):
+    def step(self, grads, master, m, v, p16, loss_scale, clip, hp, t, keep_sums=False):
+        """One oracle step over the slices; with keep_sums, self.sums holds each slice's
+        fp32 rank-order sums afterwards."""
         import oracle
 
         def sums(sl):
@@ -222,6 +231,7 @@ class PartitionedOracle:
             return gsum, bad, ss
 
         parts = list(self.pool.map(sums, self.slices))
+        self.sums = [p[0] for p in parts] if keep_sums else None
         sc = oracle.scalars(sum(p[1] for p in parts), sum(p[2] for p in parts), loss_scale,
                             clip, hp, t)
         list(self.pool.map(lambda i: oracle.adam(parts[i][0], master[self.slices[i]],
@@ -354,6 +364,73 @@ def gather_cpu_rate(w, seconds: float):
                        f"host threads; {done} passes in {el:.1f} s")}
 
 
+
+# ------------------------------------------------------------------------------------
+# which logical ranks each process owns
+
+DEFAULT_WORKLOAD = "zero3_13b_rank0_nd64"
+
+
+def process_span(w0, world: int, rank: int):
+    """This process's workload restricted to its logical ranks, and the scaling kind. A
+    workload whose span is one logical rank (a device that owns one shard of a ZeRO-2/3
+    group) gives process g the shard of logical rank r0 + g, so every process does the
+    same work (weak scaling); a workload whose span covers several logical ranks splits
+    them into equal contiguous pieces, one per process (strong scaling)."""
+    import sharded_emulated_reduce_gb300 as z
+    n_ranks = w0.r1 - w0.r0
+    if n_ranks == 1:
+        if w0.r0 + world > w0.nd:
+            raise SystemExit(f"--gpus {world}: the workload has {w0.nd - w0.r0} logical ranks "
+                             f"from rank {w0.r0} on")
+        g = w0.r0 + rank
+        return dataclasses.replace(w0, r0=g, r1=g + 1), "weak"
+    if n_ranks % world:
+        raise SystemExit(f"--gpus {world} must divide the span's {n_ranks} logical ranks")
+    a, b = z.rank_ranges(n_ranks, world)[rank]
+    return dataclasses.replace(w0, r0=w0.r0 + a, r1=w0.r0 + b), "strong"
+
+
+def job_params(w0, world: int) -> int:
+    """Real parameters that all processes together update in one step."""
+    return sum(process_span(w0, world, g)[0].span()[2] for g in range(world))
+
+
+def gather_layout(w) -> list:
+    """Layer offsets the gather copies: the workload's layer table (ZeRO-3), or one layer
+    holding the whole flat parameter vector (the parameter all-gather of ZeRO-1/2)."""
+    return list(w.layers) if w.layers else [0, w.n]
+
+
+def gather_flush(w) -> bool:
+    """Whether L2 could keep the gather's shards and layers between calls."""
+    return 4 * w.n < 2 * L2_NOMINAL
+
+
+def config_of(w, n_gpus):
+    """The workload as both arms name it (identical objects in the GPU and oracle lines)."""
+    first, n_span, n_valid = w.span()
+    offs = gather_layout(w)
+    weak = (w.r1 - w.r0) == 1
+    return {"workload": w.name, "n_params": w.n, "nd": w.nd, "align": w.align,
+            "stage": w.stage, "span_ranks": [w.r0, w.r1], "params_in_span": n_valid,
+            "loss_scale": w.loss_scale, "clip": w.clip,
+            "parallelism": (f"zero{w.stage} nd{w.nd}: each of {n_gpus} gpu steps one logical "
+                            f"rank's shard" if weak else
+                            f"zero{w.stage} nd{w.nd}: the span's logical ranks split over "
+                            f"{n_gpus} gpu"),
+            "gather": (f"{w.nd} fp16 shards of {w.layout()[1]:,} into {len(offs) - 1} layer "
+                       f"buffers" if w.layers else
+                       f"{w.nd} fp16 shards into one flat buffer of {w.n:,} (ZeRO-1/2)"),
+            "l2": ("inputs larger than L2 (two alternating gradient sets of "
+                   f"{2 * w.nd * n_span / 1e9:.2f} GB each); no flush" if not l2_flush(w)
+                   else f"working set {working_set(w) / 1e6:.0f} MB < 2 x L2: L2 flushed (a "
+                        f"write of twice the L2 size) before every step, outside the step's "
+                        f"events"),
+            "io": "fp16 grads in, fp32 master/m/v, fp16 params out",
+            "state": "HBM"}
+
+
 def run_reference(args, w):
     rank = env_int("RANK", 0)
     if rank != 0:
@@ -373,30 +450,18 @@ def run_reference(args, w):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "strong",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(w, args.gpus),
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": process_span(w, 1, 0)[1], "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config_of(w, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if not args.no_gather and args.cpu_seconds > 0:
+        g = gather_cpu_rate(w, min(args.cpu_seconds, 6.0))
+        line["gather"] = {"value": g["value"], "unit": g["unit"], "cpu_baseline": g}
     print(json.dumps(line))
     return 0
-
-
-def config_of(w, n_gpus):
-    first, n_span, n_valid = w.span()
-    return {"workload": w.name, "n_params": w.n, "nd": w.nd, "align": w.align,
-            "stage": w.stage, "span_ranks": [w.r0, w.r1], "params_in_span": n_valid,
-            "loss_scale": w.loss_scale, "clip": w.clip,
-            "parallelism": f"zero{w.stage} nd{w.nd} on {n_gpus} gpu",
-            "l2": ("inputs larger than L2 (two alternating gradient sets of "
-                   f"{2 * w.nd * n_span / 1e9:.2f} GB each); no flush" if not l2_flush(w)
-                   else f"working set {working_set(w) / 1e6:.0f} MB < 2 x L2: L2 flushed (a "
-                        f"write of twice the L2 size) before every step, outside the step's "
-                        f"events"),
-            "io": "fp16 grads in, fp32 master/m/v, fp16 params out",
-            "state": "HBM"}
 
 
 # ------------------------------------------------------------------------------------
@@ -417,11 +482,7 @@ def run_ours(args, w0):
         dist.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
-    # split the workload's own span of logical ranks across the processes
-    if (w0.r1 - w0.r0) % world:
-        raise SystemExit(f"--gpus {world} must divide the span's {w0.r1 - w0.r0} logical ranks")
-    r0, r1 = [(w0.r0 + a, w0.r0 + b) for a, b in z.rank_ranges(w0.r1 - w0.r0, world)][rank]
-    w = dataclasses.replace(w0, r0=r0, r1=r1)
+    w, scaling = process_span(w0, world, rank)
     first, n_span, n_valid = w.span()
     dev = torch.device("cuda", torch.cuda.current_device())
 
@@ -434,6 +495,7 @@ def run_ours(args, w0):
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
     z.zero_plan_bind(plan, w.r0, w.r1, master, m, v, p16, ws, 0)
     stream = torch.cuda.current_stream()
+
     def one_step(grads):
         if dist is None:
             z.zero_shard_step(plan, w.r0, w.r1, grads, w.loss_scale, w.clip, stream)
@@ -470,39 +532,50 @@ def run_ours(args, w0):
             dist.barrier()
         torch.cuda.synchronize()
 
+    def job_max(x: float) -> float:
+        """The largest value of x over all processes."""
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        if dist is not None:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.item()
+
     for i in range(args.warmup):
         one_step(gsets[i % len(gsets)])
     barrier()
 
-    # A working set that L2 could hold between steps (the gradient sets and the state)
-    # gets an L2 flush before every step: a write of twice the L2 size, outside the step's
-    # own events; the step time is then the sum of the per-step event intervals.
+    # A working set that L2 could hold between iterations gets an L2 flush before every
+    # iteration: a write of twice the L2 size, outside the iteration's own events; the
+    # time is then the sum of the per-iteration event intervals.
     flush_buf = (torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
-                 if l2_flush(w0) else None)
+                 if l2_flush(w0) or (not args.no_gather and gather_flush(w0)) else None)
 
-    def timed_steps():
-        """K steps between events on the launching stream; returns milliseconds."""
+    def timed(body, count, flush):
+        """`count` iterations of body(i) between events on the launching stream; returns
+        milliseconds."""
         barrier()
-        if flush_buf is None:
+        if not flush:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for i in range(args.steps):
-                one_step(gsets[i % len(gsets)])
+            for i in range(count):
+                body(i)
             e1.record(stream)
             barrier()
             return e0.elapsed_time(e1)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        # hold the stream for a moment so that the host queues the steps ahead of the GPU:
-        # each step's events then bracket device work only, not waits for the host
+              for _ in range(count)]
+        # hold the stream for a moment so that the host queues the iterations ahead of the
+        # GPU: each iteration's events then bracket device work only, not host waits
         torch.cuda._sleep(HOLD_CYCLES)
-        for i in range(args.steps):
+        for i in range(count):
             flush_buf.zero_()
             ev[i][0].record(stream)
-            one_step(gsets[i % len(gsets)])
+            body(i)
             ev[i][1].record(stream)
         barrier()
         return sum(a.elapsed_time(b) for a, b in ev)
+
+    def step_body(i):
+        one_step(gsets[i % len(gsets)])
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -512,88 +585,69 @@ def run_ours(args, w0):
     # kernel's average duration (the roofline). The events themselves add a few
     # microseconds per step, which is why the step time is taken without them.
     clocks.mark("start")
-    ms_total = timed_steps()
+    ms_total = timed(step_body, args.steps, l2_flush(w0))
     z.zero_profile_read(plan, reset=True)
     z.zero_profile_enable(plan, True)
-    ms_profiled = timed_steps() if graphs is None else None  # replays carry no events
+    ms_profiled = timed(step_body, args.steps, l2_flush(w0)) if graphs is None else None
     clocks.mark("end")
     z.zero_profile_enable(plan, False)
     kms, klaunch = z.zero_profile_read(plan, reset=True)
-    clk = clocks.stop()
     info = z.zero_step_result(plan).as_dict()
 
-    ms = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    ms_per_step = ms.item() / args.steps
-    total_params = w0.span()[2]
+    ms_per_step = job_max(ms_total) / args.steps
+    total_params = job_params(w0, world)
     value = total_params / (ms_per_step / 1e3)
 
-    # e2e through the public API with host buffers. Three ways a user can feed the step
-    # from pinned host memory, each timed over whole steps, every step including the
-    # upload of its own gradients and the read-back of its result: "copy" stages the
-    # gradients into HBM with cudaMemcpyAsync and then steps; "copy_overlap" does the same
-    # through two device buffers, uploading step i+1's gradients on a second stream while
-    # step i runs; "zero_copy" passes the pinned host pointers to the step, whose reduce
-    # kernel reads them over NVLink-C2C directly.
-    e2e_steps = 0
-    e2e_modes = {}
-    if not args.no_e2e:
-        host = [[g.cpu().pin_memory() for g in gs] for gs in gsets]
-        dev_g = [[torch.empty_like(g) for g in gsets[0]] for _ in range(2)]
-        e2e_steps = max(3, min(args.steps, 100))
-        copy_stream = torch.cuda.Stream()
-        uploaded = [torch.cuda.Event() for _ in range(2)]
-        consumed = [torch.cuda.Event() for _ in range(2)]
+    e2e = run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world,
+                  total_params) if not args.no_e2e else None
 
-        def upload(i, buf):  # step i's gradients into buf, on the current stream
-            for d, h in zip(buf, host[i % len(host)]):
-                d.copy_(h, non_blocking=True)
+    gather = hot = None
+    if not args.no_gather:
+        # the parameter gather after the step: the span's own shards are the step's fp16
+        # output, the other ranks' shards are seeded
+        offs = gather_layout(w0)
+        shards = wl.span_shards(w, p16, dev)
+        dst = [torch.empty(offs[l + 1] - offs[l], dtype=torch.float16, device=dev)
+               for l in range(len(offs) - 1)]
 
-        def run_mode(mode, n):
-            """n steps of `mode`, from the first upload to the last result read."""
-            if mode == "copy_overlap":
-                # buffer b = i % 2: upload i waits until step i-2 has consumed buffer b
-                with torch.cuda.stream(copy_stream):
-                    upload(0, dev_g[0])
-                    uploaded[0].record(copy_stream)
-                for i in range(n):
-                    b = i % 2
-                    if i + 1 < n:
-                        nb = (i + 1) % 2
-                        with torch.cuda.stream(copy_stream):
-                            if i >= 1:
-                                copy_stream.wait_event(consumed[nb])
-                            upload(i + 1, dev_g[nb])
-                            uploaded[nb].record(copy_stream)
-                    stream.wait_event(uploaded[b])
-                    one_step(dev_g[b])
-                    consumed[b].record(stream)
-                    z.zero_step_result(plan)
-                return
-            for i in range(n):
-                if mode == "copy":
-                    upload(i, dev_g[0])
-                    one_step(dev_g[0])
-                else:
-                    one_step(host[i % len(host)])
-                z.zero_step_result(plan)
+        def gather_body(i):
+            z.zero_gather_layers(plan, offs, shards, dst, stream)
 
-        for mode in ("copy", "copy_overlap", "zero_copy"):
-            run_mode(mode, 2)
-            barrier()
-            t0 = time.perf_counter()
-            run_mode(mode, e2e_steps)
-            barrier()
-            sec = torch.tensor([(time.perf_counter() - t0) / e2e_steps], dtype=torch.float64,
-                               device=dev)
-            if dist is not None:
-                dist.all_reduce(sec, op=dist.ReduceOp.MAX)
-            e2e_modes[mode] = total_params / sec.item()
-        del host, dev_g
-    e2e_best = max(e2e_modes, key=e2e_modes.get) if e2e_modes else None
-    e2e_value = e2e_modes.get(e2e_best) if e2e_best else None
-    h2d = sum(g.numel() * g.element_size() for g in gsets[0]) * world
+        for i in range(3):
+            gather_body(i)
+        barrier()
+        z.zero_profile_read(plan, reset=True)
+        z.zero_profile_enable(plan, True)
+        clocks.mark("start")
+        gms = timed(gather_body, args.steps, gather_flush(w0))
+        clocks.mark("end")
+        z.zero_profile_enable(plan, False)
+        gk_ms, gk_n = z.zero_profile_read(plan, reset=True)
+        if z.zero_gather_status(plan) != 0:
+            raise SystemExit("the gather reported a device failure")
+        gather = gather_object(w0, offs, args.steps, job_max(gms) / args.steps,
+                               gk_ms[z.PROF_GATHER], gk_n[z.PROF_GATHER], world,
+                               traffic=load_traffic("gather", w0))
+        if rank == 0 and args.cpu_seconds > 0:
+            gather["cpu_baseline"] = gather_cpu_rate(w0, min(args.cpu_seconds, 6.0))
+
+        # one pass of the whole hot path: the step, then the gather of its output
+        def pass_body(i):
+            step_body(i)
+            gather_body(i)
+
+        n_pass = max(3, min(args.steps, 50))
+        for i in range(2):
+            pass_body(i)
+        clocks.mark("start")
+        pms = timed(pass_body, n_pass, l2_flush(w0) or gather_flush(w0))
+        clocks.mark("end")
+        hot = {"ms_per_pass": job_max(pms) / n_pass, "passes": n_pass,
+               "what": "one shard step of the span, then the gather of all shards (the "
+                       "step's fp16 output among them) into the layer buffers",
+               "ms_step_plus_gather_timed_apart": ms_per_step + gather["ms_per_call"]}
+        del shards, dst
+    clk = clocks.stop()
 
     peak, peak_kind = load_peaks()
     n_real = n_valid
@@ -631,31 +685,34 @@ def run_ours(args, w0):
     moved = (2 * w0.nd + 34) * total_params / (ms_per_step / 1e3) / 1e9
 
     if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        plan.close()
         return 0
     cpu = oracle_sample_rate(w0, args.cpu_seconds) if args.cpu_seconds > 0 else None
     cfg = config_of(w0, world)
-    cfg["timing"] = ("K steps between two events on the launching stream, without the "
-                     "library's per-launch events (a second pass with them gives the "
-                     "per-kernel durations)")
-    if graphs is not None:
-        cfg["launch"] = "CUDA graph replay (one graph per gradient set)"
     if args.state == "host":
         cfg["state"] = ("master/m/v in pinned Grace memory over NVLink-C2C; fp16 parameters "
                         "in HBM")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": scaling, "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": cfg,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": STEP_INFO_D2H_BYTES * world, "steps": e2e_steps,
-                "mode": e2e_best, "by_mode": e2e_modes},
+        "timing": ("K steps between two events on the launching stream, without the "
+                   "library's per-launch events (a second pass with them gives the "
+                   "per-kernel durations); max over processes"),
+        "launch": ("CUDA graph replay (one graph per gradient set)" if graphs is not None
+                   else "eager calls through the C ABI"),
+        "e2e": e2e,
         "gpu_launches": launches,
         "roofline": roofline,
         "step_hbm": {"alg_bytes_per_param": 2 * w0.nd + 26, "alg_gbs": step_gbs,
                      "alg_frac": step_gbs / peak,
                      "min_moved_bytes_per_param": 2 * w0.nd + 34, "min_moved_gbs": moved,
                      "min_moved_frac": moved / peak, "peak": peak, "peak_kind": peak_kind},
+        "gather": gather,
+        "hot_path": hot,
         "cpu_baseline": cpu,
         "clocks": clk,
         "last_step": {k: info[k] for k in ("step", "skipped", "global_norm", "clip_coef")},
@@ -665,6 +722,114 @@ def run_ours(args, w0):
         dist.destroy_process_group()
     plan.close()
     return 0
+
+
+E2E_LINK_GBS = 200.0  # host-to-device rate used only to size the end-to-end leg
+E2E_SECONDS = 3.0     # about this long per end-to-end mode
+
+
+def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world,
+            total_params):
+    """The step end to end through the public API from pinned host memory, in the ways a
+    user can feed it, each timed over whole steps; every step includes the upload of its
+    gradients and the read-back of its result (the step info: flag, skip, norm, counter).
+    One pinned gradient set is reused for every step. "copy" stages the gradients into
+    HBM with cudaMemcpyAsync and then steps; "copy_overlap" does the same through two
+    device buffers, uploading step i+1's gradients on a second stream while step i runs;
+    "zero_copy" passes the pinned host pointers to the step, whose reduce kernel reads
+    them over NVLink-C2C directly. A fourth leg, "copy" plus a read-back of the fp16
+    parameters to pinned host memory each step, is reported beside them."""
+    import torch
+
+    import sharded_emulated_reduce_gb300 as z
+    host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gsets[0]]
+    for h, g in zip(host, gsets[0]):
+        h.copy_(g)
+    dev_g = [[torch.empty_like(g) for g in gsets[0]] for _ in range(2)]
+    p16_host = torch.empty(p16.numel(), dtype=p16.dtype, pin_memory=True)
+    h2d_rank = sum(g.numel() * g.element_size() for g in gsets[0])
+    est = h2d_rank / (E2E_LINK_GBS * 1e9)
+    steps = max(3, min(args.steps, 100, int(E2E_SECONDS / max(est, 1e-6))))
+    copy_stream = torch.cuda.Stream()
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+
+    def upload(buf):  # the gradients into buf, on the current stream
+        for d, h in zip(buf, host):
+            d.copy_(h, non_blocking=True)
+
+    def run_mode(mode, n):
+        """n steps of `mode`, from the first upload to the last result read."""
+        if mode == "copy_overlap":
+            # buffer b = i % 2: upload i waits until step i-2 has consumed buffer b
+            with torch.cuda.stream(copy_stream):
+                upload(dev_g[0])
+                uploaded[0].record(copy_stream)
+            for i in range(n):
+                b = i % 2
+                if i + 1 < n:
+                    nb = (i + 1) % 2
+                    with torch.cuda.stream(copy_stream):
+                        if i >= 1:
+                            copy_stream.wait_event(consumed[nb])
+                        upload(dev_g[nb])
+                        uploaded[nb].record(copy_stream)
+                stream.wait_event(uploaded[b])
+                one_step(dev_g[b])
+                consumed[b].record(stream)
+                z.zero_step_result(plan)
+            return
+        for i in range(n):
+            if mode == "zero_copy":
+                one_step(host)
+            else:
+                upload(dev_g[0])
+                one_step(dev_g[0])
+            if mode == "copy_params_to_host":
+                p16_host.copy_(p16, non_blocking=True)
+            z.zero_step_result(plan)
+
+    rates = {}
+    for mode in ("copy", "copy_overlap", "zero_copy", "copy_params_to_host"):
+        run_mode(mode, 2)
+        barrier()
+        t0 = time.perf_counter()
+        run_mode(mode, steps)
+        barrier()
+        rates[mode] = total_params / job_max((time.perf_counter() - t0) / steps)
+    del host, dev_g
+    with_params = rates.pop("copy_params_to_host")
+    best = max(rates, key=rates.get)
+    h2d = h2d_rank * world
+    p16_bytes = p16.numel() * p16.element_size() * world
+    return {"value": rates[best], "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": STEP_INFO_D2H_BYTES * world, "steps": steps, "mode": best,
+            "by_mode": rates,
+            "result_read_back": ("the step info (overflow flag, skip, norm, step counter) "
+                                 "each step; the fp16 parameters stay in HBM, where the "
+                                 "forward pass and the gather read them"),
+            "with_params_to_host": {"value": with_params, "unit": UNIT, "mode": "copy",
+                                    "h2d_bytes_per_step": h2d,
+                                    "d2h_bytes_per_step": p16_bytes + STEP_INFO_D2H_BYTES * world}}
+
+
+def gather_object(w, offs, calls, ms_per_call, kernel_ms, launches, world, traffic=None):
+    """The gather's figures: parameters moved per second (all processes), and its kernels'
+    achieved HBM bandwidth (4 algorithmic bytes per parameter over their summed
+    per-launch durations) against the measured peak."""
+    peak, peak_kind = load_peaks()
+    n_moved = offs[-1] - offs[0]
+    alg_total = 4 * n_moved * calls
+    achieved = alg_total / (kernel_ms / 1e3) / 1e9
+    per_call = launches / calls
+    return {"value": world * n_moved / (ms_per_call / 1e3), "unit": "params/s",
+            "ms_per_call": ms_per_call, "calls": calls, "params_per_call": n_moved,
+            "layers": len(offs) - 1, "gpu_launches": int(launches) * world,
+            "roofline": {"bound": "hbm", "kernel": "gather", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": traffic,
+                         "alg_bytes_per_launch": 4 * n_moved / per_call,
+                         "avg_launch_ms": kernel_ms / launches}}
 
 
 KERNEL_SOURCES = ("step_kernels.cu", "gather_kernel.cu", "bulk_async.h", "grid_sync.h",
@@ -697,10 +862,12 @@ def load_traffic(kernel: str, w):
     ent = d.get("workloads", {}).get(w.name, {}).get(kernel)
     return None if not ent else ent.get("dram_bytes_per_launch")
 
+
 def run_gather(args, w):
-    """Time the gather of all Nd fp16 shards into the workload's layer buffers (ZeRO-3),
-    or, for a workload without a layer table, into one buffer holding the whole flat
-    parameter vector (the parameter all-gather of ZeRO-1/2)."""
+    """Time the gather alone: all Nd fp16 shards into the workload's layer buffers
+    (ZeRO-3), or, for a workload without a layer table, into one buffer holding the whole
+    flat parameter vector (the parameter all-gather of ZeRO-1/2). With --prefetch, layer
+    by layer with one completion event per layer."""
     import torch
 
     import sharded_emulated_reduce_gb300 as z
@@ -713,7 +880,7 @@ def run_gather(args, w):
     shard0 = torch.empty(s, dtype=torch.float16, device="cuda")
     shards = wl.make_shards(w, shard0)
     wl.fill(shard0, wl.key(w, wl.SHARD16, 0, 0), w.shard_sigma, start=0, n_valid=w.n)
-    offs = list(w.layers) if w.layers else [0, w.n]  # ZeRO-1/2: one full-buffer layer
+    offs = gather_layout(w)
     if args.layer_shift:
         # move every interior layer boundary by a few elements: layers then start at
         # addresses misaligned (mod 16 bytes) relative to the shards they copy from
@@ -722,10 +889,11 @@ def run_gather(args, w):
            for l in range(len(offs) - 1)]
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
     stream = torch.cuda.current_stream()
+    events = z.make_layer_events(len(offs) - 1) if args.prefetch else None
 
     def gather():
-        if args.prefetch:  # one launch and one event per layer
-            return z.zero_prefetch_layers(plan, offs, shards, dst, stream)
+        if args.prefetch:  # one launch and one event per layer, from one C call
+            return z.zero_gather_layers_events(plan, offs, shards, dst, events, stream)
         return z.zero_gather_layers(plan, offs, shards, dst, stream)
 
     for _ in range(args.warmup):
@@ -748,39 +916,37 @@ def run_gather(args, w):
     prefetch = None
     if args.prefetch:
         # when each layer is ready, counted from the call (one more call, after the timing)
+        timing_events = z.make_layer_events(len(offs) - 1, timing=True)
         t0 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        evs = z.zero_prefetch_layers(plan, offs, shards, dst, stream, timing=True)
+        z.zero_gather_layers_events(plan, offs, shards, dst, timing_events, stream)
         torch.cuda.synchronize()
-        ready = [t0.elapsed_time(e) for e in evs]
+        ready = [t0.elapsed_time(e) for e in timing_events]
         prefetch = {"layer_ready_ms": ready, "first_layer_ms": ready[0],
                     "all_layers_ms": ready[-1]}
     ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.stop()
-    n_moved = offs[-1] - offs[0]
-    peak, peak_kind = load_peaks()
-    avg = kms[z.PROF_GATHER] / kl[z.PROF_GATHER]  # per launch
-    launches_per_call = kl[z.PROF_GATHER] // args.steps
-    alg = 4 * n_moved / launches_per_call
-    achieved = alg / (avg / 1e3) / 1e9
+    # with --prefetch consecutive layers overlap on two streams, so their per-launch
+    # durations overlap too: the bandwidth is taken over whole calls instead
+    g = gather_object(w, offs, args.steps, ms,
+                      ms * args.steps if args.prefetch else kms[z.PROF_GATHER],
+                      kl[z.PROF_GATHER], 1,
+                      traffic=(None if args.layer_shift or args.prefetch
+                               else load_traffic("gather", w)))
+    if args.prefetch:
+        g["roofline"]["timed"] = "whole calls (layers overlap on two streams)"
     line = {
         "metric": "ZeRO-3 gather params/s (fp16 shards to layer buffers); achieved HBM GB/s "
                   "as % of GB300 peak",
-        "value": n_moved / (ms / 1e3), "unit": "params/s", "n_gpus": 1, "steps": args.steps,
+        "value": g["value"], "unit": "params/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
         "vs_baseline": None, "dtype": "f16 (copy)", "data": "synthetic",
         "config": {"workload": w.name, "op": "gather", "n_params": w.n, "nd": w.nd,
                    "layer_shift": args.layer_shift, "prefetch": bool(args.prefetch),
                    "layers": len(offs) - 1, "shard_len": s,
                    "l2": f"inputs larger than L2 ({2 * w.n / 1e9:.1f} GB of shards); no flush"},
-        "e2e": None, "gpu_launches": int(kl[z.PROF_GATHER]),
-        "roofline": {"bound": "hbm", "kernel": "gather", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                     # the stored capture is of one aligned whole-buffer launch
-                     "traffic": (None if args.layer_shift or args.prefetch
-                                 else load_traffic("gather", w)),
-                     "alg_bytes_per_launch": alg,
-                     "avg_launch_ms": avg},
+        "e2e": None, "gpu_launches": g["gpu_launches"],
+        "roofline": g["roofline"],
         "cpu_baseline": (gather_cpu_rate(w, args.cpu_seconds) if args.cpu_seconds > 0
                          else None),
         "clocks": clk,
@@ -796,20 +962,23 @@ def main(argv=None):
     from synth import workloads as wl
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gpt2_small_flat_nd8", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--op", default="step", choices=["step", "gather"],
-                    help="the shard step (default) or the ZeRO-3 gather")
+                    help="the shard step with the gather after it (default), or the gather "
+                         "alone")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU oracle baseline budget (0 skips it)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--no-gather", action="store_true",
+                    help="step: leave out the gather and the step + gather pass")
     ap.add_argument("--state", default="device", choices=["device", "host"],
                     help="where master/m/v live: HBM, or pinned Grace memory read and "
                          "written over NVLink-C2C (the fp16 parameters stay in HBM)")
     ap.add_argument("--prefetch", action="store_true",
-                    help="gather: one launch and one event per layer (zero_prefetch_layers)")
+                    help="gather: one launch and one completion event per layer")
     ap.add_argument("--layer-shift", type=int, default=0,
                     help="gather: shift interior layer boundaries by this many elements")
     ap.add_argument("--graph", action="store_true",

@@ -127,15 +127,24 @@ int zero_plan_create(int64_t n_params, int32_t nd, int32_t stage, int32_t align,
  * touched. Any work enqueued with the plan must have completed. */
 void zero_plan_destroy(zero_plan* plan);
 
-/* The plan's padded length Np and shard length S (shard r starts at r * S). */
+/* The plan's padded length Np and shard length S (shard r starts at r * S): the partition
+ * of the flat buffer into Nd equal shards ("ZeRO" method entry, description; ZeRO
+ * explainer, Chapter 02 "What each stage shards"), as zero_plan_create defines it. Host
+ * only. Errors: ZERO_EINVAL (a NULL argument). */
 int zero_plan_layout(const zero_plan* plan, int64_t* padded_len, int64_t* shard_len);
 
 /* Bytes of fp32 workspace the step needs for the span of logical ranks [r0, r1):
- * 4 * (r1 - r0) * S. Returns the byte count, or a negative ZERO_E* code. */
+ * 4 * (r1 - r0) * S, the span's summed gradients. The pages count the fp32 gradient copy
+ * as transient, not as model state (ZeRO explainer, "The 16 Bytes per Parameter Audit":
+ * 2 + 2 + 12 bytes per parameter); this is where it lives between the sum and the
+ * update. Host only. Returns the byte count, or ZERO_EINVAL. */
 int64_t zero_workspace_bytes(const zero_plan* plan, int32_t r0, int32_t r1);
 
 /* Bind the optimizer state of the span [r0, r1) (0 <= r0 < r1 <= nd; n = (r1-r0)*S
- * elements, element i is flat index r0*S + i):
+ * elements, element i is flat index r0*S + i). These are the partitioned model states a
+ * ZeRO rank keeps for its own partition only: the fp32 master weights, momentum and
+ * variance (12 bytes per parameter) and the fp16 parameter copy (ZeRO explainer, "The 16
+ * Bytes per Parameter Audit" and Chapter 02 "What each stage shards"):
  *   master, exp_avg, exp_avg_sq: fp32[n], device, read and written by the step;
  *   param16: fp16[n], device, written by the step (the fp16 parameter copy);
  *   workspace: zero_workspace_bytes(plan, r0, r1) bytes of device memory, scratch;
@@ -195,8 +204,12 @@ int zero_shard_stats(zero_plan* plan, void** dev_words);
 int zero_shard_update(zero_plan* plan, int32_t r0, int32_t r1, float loss_scale, float clip,
                       void* stream);
 
-/* Wait for the plan's last step to finish and copy its result to *out. This is the
- * only call that synchronises with the device. Errors: ZERO_EINVAL, ZERO_EUNBOUND (no
+/* Wait for the plan's last step to finish and copy its result to *out: the overflow
+ * flag and skip decision of the mixed-precision step (ZeRO explainer, "The
+ * mixed-precision era" and Chapter 02 "Memory per parameter": fp16 gradients with fp32
+ * master state; an inf/nan gradient skips the update), the global norm and clip
+ * coefficient, the step counter and the device-side failure status. This is the only
+ * step call that synchronises with the device. Errors: ZERO_EINVAL, ZERO_EUNBOUND (no
  * step yet), ZERO_ECUDA, ZERO_EDEVICE (out is still filled). */
 int zero_step_result(zero_plan* plan, zero_step_info* out);
 
@@ -215,9 +228,35 @@ int zero_step_result(zero_plan* plan, zero_step_info* out);
  * by a kernel that realigns 16-byte blocks in registers (same result, same traffic).
  * Enqueued on stream. The first call on a plan that was never bound allocates the
  * plan's small device scratch (which holds the gather's status word) on the current
- * device. Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+ * device. The plan is not const: the call may allocate that scratch, and it records the
+ * stream it used so that zero_gather_status can wait for it.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
 int zero_gather_layers(zero_plan* plan, const int64_t* layer_offsets, int32_t n_layers,
                        const void* const* shard_ptrs, void* const* layer_dst, void* stream);
+
+/* The ZeRO-3 gather layer by layer, with a completion event per layer: the "dynamic
+ * communication schedule" of the ZeRO method entry (codewithpapers.app/method/zero,
+ * description), in which the all-gather of later layers runs ahead while the work on an
+ * earlier layer starts. Copies exactly what zero_gather_layers copies, with the same
+ * arguments and checks, plus:
+ *   layer_done: host array of n_layers cudaEvent_t handles passed as void* (the caller
+ *     creates them on the plan's device and owns them; an entry may be NULL for "no
+ *     event"). layer_done[l] is recorded once layer l's copy has been enqueued, so
+ *     cudaStreamWaitEvent(other_stream, layer_done[l]) lets other work start on layer l
+ *     while later layers are still being copied.
+ * Layers are enqueued in order, each by its own launch(es): layers 0, 2, 4, ... on
+ * `stream`, layers 1, 3, 5, ... on a second stream that the plan owns, which first waits
+ * for the work already on `stream` and is joined back into `stream` at the end. So two
+ * consecutive layers may run at the same time (the next one takes the SMs the previous
+ * one leaves, which hides each launch's start and end), and layer_done[l] marks layer l
+ * alone: it may complete before layer_done[l-1]. Work enqueued on `stream` after this call
+ * starts after every layer; zero_gather_status covers the call. An event handle that is
+ * not valid on the plan's device makes the call fail with ZERO_ECUDA after the earlier
+ * layers have been enqueued (their copies still complete, and `stream` is still joined).
+ * Errors: ZERO_EINVAL (also for layer_done == NULL), ZERO_EALIGN, ZERO_ECUDA. */
+int zero_gather_layers_events(zero_plan* plan, const int64_t* layer_offsets, int32_t n_layers,
+                              const void* const* shard_ptrs, void* const* layer_dst,
+                              void* const* layer_done, void* stream);
 
 /* Wait for the plan's last gather and report whether it finished (the library's own
  * failure reporting; the pages have no counterpart): *status is 0, or 4 if a
@@ -232,7 +271,11 @@ int zero_gather_status(zero_plan* plan, int32_t* status);
  * shard length of create's partition:
  *   stage 0 (plain data parallel) 16 N; stage 1 4 N + 12 S; stage 2 2 N + 14 S;
  *   stage 3 16 S.
- * Host only. Errors: ZERO_EINVAL. */
+ * align (elements, >= 1) is an argument because a rank holds its whole padded shard:
+ * S = Np / nd with Np = ceil(n_params / (nd * align)) * nd * align, as zero_plan_create
+ * partitions, so the same n_params and nd give different per-rank bytes for different
+ * alignments (for align = 1 and nd dividing n_params, S = n_params / nd exactly, the
+ * pages' Psi / Nd). Host only. Errors: ZERO_EINVAL. */
 int zero_memory_bytes(int64_t n_params, int32_t nd, int32_t align, int32_t stage,
                       int64_t* per_rank_bytes);
 
@@ -270,7 +313,8 @@ int zero_profile_read(zero_plan* plan, double* ms, int64_t* launches, int32_t re
  * caches it; make that first call before any stream capture. Every call shares the array
  * and it keeps the last call's contents (the control words that must start at zero are
  * cleared by each call), so calls whose work overlaps on the GPU race and give wrong
- * results: order them on one stream or with events. Enqueued on stream; asynchronous.
+ * results: order them on one stream or with events. Enqueued on stream; asynchronous: a
+ * device-side failure is reported only through zero_noalloc_step_result.
  * Errors: ZERO_EINVAL (including n > ZERO_NOALLOC_MAX_SPAN), ZERO_EALIGN, ZERO_ECUDA;
  * nothing is launched on an error. */
 #define ZERO_NOALLOC_MAX_SPAN 4194304
@@ -278,6 +322,19 @@ int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid, const void* 
                             float* master, float* exp_avg, float* exp_avg_sq, void* param16,
                             int64_t* step_counter, const zero_adam_hparams* hp,
                             float loss_scale, float clip, void* stream);
+
+/* Result of the last allocation-free step on the current device (a companion of
+ * zero_shard_step_noalloc; the pages have no counterpart). Waits for `stream` (the stream
+ * that step was enqueued on), then copies the step's overflow flag, skip decision, norm,
+ * clip coefficient, scalars and step counter, and its device-side failure status, from the
+ * library's scratch array into *out. This is the only way to see a failure inside that
+ * step: status 2 (a bulk load of the update did not arrive within its bounded wait) or 5
+ * (the grid barrier of the one-launch step gave up, so parts of the span may be updated and
+ * others not); the step call itself returns ZERO_OK once its work is enqueued. Allocates
+ * nothing. The array holds the result of whichever allocation-free step ran last on the
+ * device. Errors: ZERO_EINVAL, ZERO_EUNBOUND (no allocation-free step has run on the
+ * current device), ZERO_ECUDA, ZERO_EDEVICE (status != 0; *out is still filled). */
+int zero_noalloc_step_result(void* stream, zero_step_info* out);
 
 /* Configure the plan's device-resident loss scaler (see zero_loss_scaler) after
  * zero_plan_bind. While it is on, zero_shard_step and zero_shard_update must be given

@@ -86,6 +86,8 @@ _SIGS = {
     "zero_shard_update": ([_P, _I32, _I32, _F, _F, _P], ctypes.c_int),
     "zero_step_result": ([_P, ctypes.POINTER(zero_step_info)], ctypes.c_int),
     "zero_gather_layers": ([_P, ctypes.POINTER(_I64), _I32, _PP, _PP, _P], ctypes.c_int),
+    "zero_gather_layers_events": ([_P, ctypes.POINTER(_I64), _I32, _PP, _PP, _PP, _P],
+                                  ctypes.c_int),
     "zero_memory_bytes": ([_I64, _I32, _I32, _I32, ctypes.POINTER(_I64)], ctypes.c_int),
     "zero_gather_status": ([_P, ctypes.POINTER(_I32)], ctypes.c_int),
     "zero_profile_enable": ([_P, _I32], ctypes.c_int),
@@ -93,6 +95,7 @@ _SIGS = {
                           ctypes.c_int),
     "zero_shard_step_noalloc": ([_I32, _I64, _I64, _PP, _P, _P, _P, _P, _P,
                                  ctypes.POINTER(zero_adam_hparams), _F, _F, _P], ctypes.c_int),
+    "zero_noalloc_step_result": ([_P, ctypes.POINTER(zero_step_info)], ctypes.c_int),
     "zero_plan_set_scaler": ([_P, ctypes.POINTER(zero_loss_scaler)], ctypes.c_int),
     "zero_loss_scale_ptr": ([_P, ctypes.POINTER(_P)], ctypes.c_int),
     "zero_plan_get_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
@@ -353,6 +356,14 @@ def zero_shard_step_noalloc(nd: int, n: int, n_valid: int, grads: Sequence, mast
                                         clip, _stream(stream)))
 
 
+def zero_noalloc_step_result(stream=None) -> zero_step_info:
+    """Result of the last allocation-free step on the current device (waits for
+    ``stream``); raises ZeroError with ZERO_EDEVICE if that step reported a failure."""
+    info = zero_step_info()
+    _check(_lib.zero_noalloc_step_result(_stream(stream), ctypes.byref(info)))
+    return info
+
+
 # ------------------------------------------------------------------------------------
 # Dynamic loss scale and checkpoints
 
@@ -432,25 +443,52 @@ def torch_uint8():
 # ------------------------------------------------------------------------------------
 # Layer-by-layer gather with completion events (ZeRO-3 prefetch)
 
-def zero_prefetch_layers(plan: Plan, layer_offsets: Sequence[int], shards: Sequence,
-                         layer_dst: Sequence, stream=None, first: int = 0,
-                         count: int | None = None, timing: bool = False) -> list:
-    """Gather layers ``first .. first+count-1`` one launch each on ``stream`` and return one
-    torch.cuda.Event per layer, recorded right after that layer's copy (with ``timing``,
-    events that can be timed). A consumer stream that waits on event l can start on layer
-    l while later layers are still being gathered: the "dynamic communication schedule"
-    of the ZeRO method entry, in which the all-gather of the next layers runs ahead of the
-    work on the current one."""
+def make_layer_events(n: int, timing: bool = False) -> list:
+    """n torch.cuda.Event objects with their CUDA events already created (recorded once on
+    the current stream), ready to be passed to zero_gather_layers_events."""
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    n_layers = len(layer_offsets) - 1
-    last = n_layers if count is None else min(n_layers, first + count)
-    events = []
-    for l in range(first, last):
-        zero_gather_layers(plan, layer_offsets[l:l + 2], shards, [layer_dst[l]], s)
-        ev = torch.cuda.Event(enable_timing=timing)
+    evs = [torch.cuda.Event(enable_timing=timing) for _ in range(n)]
+    s = torch.cuda.current_stream()
+    for ev in evs:
         ev.record(s)
-        events.append(ev)
+    return evs
+
+
+def _event_handle(ev) -> int:
+    if ev is None:
+        return 0
+    if isinstance(ev, int):
+        return ev
+    h = int(ev.cuda_event)
+    if not h:
+        raise ZeroError(ZERO_EINVAL, "event has no CUDA event yet: record it once first "
+                                     "(make_layer_events does)")
+    return h
+
+
+def zero_gather_layers_events(plan: Plan, layer_offsets: Sequence[int], shards: Sequence,
+                              layer_dst: Sequence, events: Sequence, stream=None) -> None:
+    """The gather layer by layer; events[l] (a torch.cuda.Event made by make_layer_events,
+    a raw cudaEvent_t address, or None) is recorded when layer l has been copied."""
+    n_layers = len(layer_offsets) - 1
+    if len(events) != n_layers:
+        raise ZeroError(ZERO_EINVAL, f"need {n_layers} events, got {len(events)}")
+    offs = (_I64 * len(layer_offsets))(*[int(x) for x in layer_offsets])
+    evs = (ctypes.c_void_p * n_layers)(*[_event_handle(e) for e in events])
+    _check(_lib.zero_gather_layers_events(plan, offs, n_layers, _ptrs(shards),
+                                          _ptrs(layer_dst), evs, _stream(stream)))
+
+
+def zero_prefetch_layers(plan: Plan, layer_offsets: Sequence[int], shards: Sequence,
+                         layer_dst: Sequence, stream=None, timing: bool = False) -> list:
+    """Gather every layer with one C call and return one torch.cuda.Event per layer,
+    recorded when that layer has been copied (with ``timing``, events that can be timed).
+    A consumer stream that waits on event l can start on layer l while later layers are
+    still being gathered: the "dynamic communication schedule" of the ZeRO method entry,
+    in which the all-gather of the next layers runs ahead of the work on the current
+    one."""
+    events = make_layer_events(len(layer_offsets) - 1, timing=timing)
+    zero_gather_layers_events(plan, layer_offsets, shards, layer_dst, events, stream)
     return events
 
 

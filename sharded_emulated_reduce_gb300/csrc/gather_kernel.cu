@@ -5,11 +5,12 @@
 // n_layers + nd of them) and numbers fixed-size tiles (64 KiB) across all segments; the
 // segment table sits in the kernel's parameter space. One persistent CTA per SM walks
 // its tiles. Where source and destination share their alignment modulo 16 bytes (every
-// layout with layer offsets that are multiples of 8 elements), one thread moves the tile
-// through a 4-stage ring of 32 KiB shared-memory buffers with TMA bulk copies: a bulk load
-// into a free buffer, then a bulk store out of it once the load has landed, several in
-// flight at once. The few elements before the first 16-byte-aligned destination address
-// and after the last are copied by the other threads. Segments whose source and
+// layout with layer offsets that are multiples of 8 elements), one thread streams the
+// 16-byte-aligned bodies of all of its tiles through a ring of 32 KiB shared-memory
+// buffers with TMA bulk copies: a bulk load into a free buffer, then a bulk store out of
+// it once the load has landed, with all but one buffer's loads in flight and no drain
+// between tiles. The few elements before the first 16-byte-aligned destination address
+// and after the last are copied by the other warps. Segments whose source and
 // destination are misaligned relative to each other go to a second kernel (the host sorts
 // them into their own table): bulk loads bring the aligned 16-byte source blocks around
 // each stretch of the tile into a shared-memory ring, and all threads recombine pairs of
@@ -22,51 +23,71 @@
 namespace zero {
 namespace {
 
-constexpr int kGatStages = 4;
-constexpr uint32_t kGatChunk = 32768;  // bytes per ring buffer
-constexpr int kGatThreads = 256;
+#ifndef ZERO_GATHER_STAGES
+#define ZERO_GATHER_STAGES 6
+#endif
+constexpr int kGatStages = ZERO_GATHER_STAGES;  // ring buffers of the aligned-copy kernel
+constexpr uint32_t kGatChunk = 32768;            // bytes per ring buffer
+constexpr int kGatThreads = 128;
 constexpr size_t kGatSmem = (size_t)kGatStages * kGatChunk + kGatStages * sizeof(uint64_t);
+static_assert(kGatStages >= 3 && kGatSmem <= 232448, "ring must fit one CTA's shared memory");
 constexpr int kMaxDevices = 64;
 
-struct Ring {
-  unsigned char* buf;
-  uint64_t* full;
-  long long q;  // chunks this CTA has moved through the ring so far
+// Geometry of one tile of the aligned-copy kernel: n elements from src to dst, the first
+// `head` elements (up to the first 16-byte-aligned destination address) and the last
+// n - head - body ones copied element by element, the `body` in between by bulk copies.
+// body = 0 when source and destination differ in alignment modulo 16 bytes (the host
+// sends such segments to the realigning kernel, so this does not occur in practice).
+struct AlTile {
+  const uint16_t* src;
+  uint16_t* dst;
+  long long n, head, body;
 };
 
-// One thread: copy `bytes` (a multiple of 16; both addresses 16-byte aligned) through the
-// ring, keeping up to kGatStages bulk loads in flight. False if a load did not arrive.
-__device__ bool ring_copy(Ring& r, const unsigned char* src, unsigned char* dst, long long bytes) {
-  const long long nch = (bytes + kGatChunk - 1) / kGatChunk;
-  const long long q0 = r.q;
-  auto len = [&](long long i) {
-    const long long left = bytes - i * (long long)kGatChunk;
-    return (uint32_t)(left < (long long)kGatChunk ? left : (long long)kGatChunk);
-  };
-  auto issue = [&](long long i) {
-    const int s = (int)((q0 + i) % kGatStages);
-    bulk_wait_read_all();  // no bulk store is still reading buffer s
-    mbar_expect_tx(&r.full[s], len(i));
-    bulk_load(r.buf + (size_t)s * kGatChunk, src + i * (long long)kGatChunk, len(i), &r.full[s]);
-  };
-  long long issued = 0;
-  while (issued < nch && issued < kGatStages) issue(issued++);
-  for (long long i = 0; i < nch; ++i) {
-    const long long q = q0 + i;
-    const int s = (int)(q % kGatStages);
-    if (!mbar_wait(&r.full[s], (uint32_t)((q / kGatStages) & 1))) {
-      for (long long k = i + 1; k < issued; ++k) {  // let the other issued loads land
-        const long long qq = q0 + k;
-        mbar_wait(&r.full[(int)(qq % kGatStages)], (uint32_t)((qq / kGatStages) & 1));
-      }
-      return false;
+__device__ __forceinline__ AlTile al_tile(const GatherLaunch& a, int& seg, long long t) {
+  while (seg + 1 < a.nseg && a.seg[seg + 1].tile_begin <= t) ++seg;
+  const GatherSeg& sg = a.seg[seg];
+  const long long e0 = (t - sg.tile_begin) * kGatherTile;
+  AlTile m;
+  m.n = sg.len - e0;
+  if (m.n > kGatherTile) m.n = kGatherTile;
+  m.src = sg.src + e0;
+  m.dst = sg.dst + e0;
+  const uintptr_t sa = reinterpret_cast<uintptr_t>(m.src);
+  const uintptr_t da = reinterpret_cast<uintptr_t>(m.dst);
+  m.head = (long long)(((16u - (unsigned)(da & 15u)) & 15u) >> 1);
+  if (m.head > m.n) m.head = m.n;
+  m.body = ((sa + 2 * m.head) & 15u) ? 0 : ((m.n - m.head) >> 3) << 3;
+  return m;
+}
+
+// Walks this CTA's bulk-copy chunks in order: its tiles blockIdx.x, + gridDim.x, ...,
+// each tile's body cut into chunks of at most kGatChunk bytes (multiples of 16 bytes,
+// 16-byte-aligned addresses).
+struct ChunkIt {
+  long long t;    // current tile
+  long long off;  // byte offset of the next chunk in the tile's body
+  int seg;
+};
+
+__device__ __forceinline__ bool next_chunk(const GatherLaunch& a, ChunkIt& it,
+                                           const unsigned char** src, unsigned char** dst,
+                                           uint32_t* len) {
+  while (it.t < a.tiles) {
+    const AlTile m = al_tile(a, it.seg, it.t);
+    const long long bytes = 2 * m.body;
+    if (it.off < bytes) {
+      const long long left = bytes - it.off;
+      *len = (uint32_t)(left < (long long)kGatChunk ? left : (long long)kGatChunk);
+      *src = reinterpret_cast<const unsigned char*>(m.src + m.head) + it.off;
+      *dst = reinterpret_cast<unsigned char*>(m.dst + m.head) + it.off;
+      it.off += *len;
+      return true;
     }
-    bulk_store(dst + i * (long long)kGatChunk, r.buf + (size_t)s * kGatChunk, len(i));
-    bulk_commit();
-    if (issued < nch) issue(issued++);
+    it.t += gridDim.x;
+    it.off = 0;
   }
-  r.q = q0 + nch;
-  return true;
+  return false;
 }
 
 // Bytes [D, D+16) of the 32-byte concatenation lo|hi, for an even D in 0..14 (little
@@ -139,47 +160,69 @@ __device__ __forceinline__ MisTile mis_tile(const GatherLaunch& L, int& seg, lon
   return m;
 }
 
-// A CTA visits its tiles in increasing order, so the segment that holds a tile is found
-// by advancing a running index through the table.
+// Thread 0 streams all of this CTA's chunks through one ring of kGatStages buffers:
+// kGatStages - 1 bulk loads stay in flight, each landed chunk leaves by a bulk store, and
+// a buffer is refilled once the store before the newest one has finished reading it. The
+// ring does not drain between tiles. Warps 1.. copy the tiles' unaligned edge elements
+// meanwhile (disjoint bytes from the bulk stores). A CTA visits its tiles in increasing
+// order, so the segment that holds a tile is found by advancing a running index.
 __global__ void __launch_bounds__(kGatThreads, 1) k_gather(const __grid_constant__ GatherLaunch a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  Ring r{smem, reinterpret_cast<uint64_t*>(smem + (size_t)kGatStages * kGatChunk), 0};
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kGatStages * kGatChunk);
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int s = 0; s < kGatStages; ++s) mbar_init(&r.full[s], 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  int seg = 0;
   bool ok = true;
-  for (long long t = blockIdx.x; t < a.tiles && ok; t += gridDim.x) {
-    while (seg + 1 < a.nseg && a.seg[seg + 1].tile_begin <= t) ++seg;
-    const GatherSeg& sg = a.seg[seg];
-    const long long e0 = (t - sg.tile_begin) * kGatherTile;
-    long long n = sg.len - e0;
-    if (n > kGatherTile) n = kGatherTile;
-    const uint16_t* src = sg.src + e0;
-    uint16_t* dst = sg.dst + e0;
-    const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
-    const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
-    long long head = (long long)(((16u - (unsigned)(da & 15u)) & 15u) >> 1);
-    if (head > n) head = n;
-    if (((sa + 2 * head) & 15u) != 0) {  // misaligned relative to each other: the host
-      for (long long i = tid; i < n; i += kGatThreads) dst[i] = src[i];  // sends none here
-      continue;
-    }
-    const long long body = ((n - head) >> 3) << 3;  // elements moved by bulk copies
-    if (tid < head) dst[tid] = src[tid];
-    const long long tail0 = head + body;
-    if (tail0 + tid < n) dst[tail0 + tid] = src[tail0 + tid];
-    if (tid == 0 && body > 0)
-      ok = ring_copy(r, reinterpret_cast<const unsigned char*>(src + head),
-                     reinterpret_cast<unsigned char*>(dst + head), body * 2);
-    ok = __syncthreads_and(ok);
-  }
   if (tid == 0) {
+    for (int s = 0; s < kGatStages; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
+    ChunkIt prod{(long long)blockIdx.x, 0, 0}, cons{(long long)blockIdx.x, 0, 0};
+    long long issued = 0, done = 0;
+    auto issue = [&]() {
+      const unsigned char* src;
+      unsigned char* dst;
+      uint32_t len;
+      if (!next_chunk(a, prod, &src, &dst, &len)) return;
+      const int s = (int)(issued % kGatStages);
+      mbar_expect_tx(&full[s], len);
+      bulk_load(smem + (size_t)s * kGatChunk, src, len, &full[s]);
+      ++issued;
+    };
+    for (int k = 0; k < kGatStages - 1; ++k) issue();
+    const unsigned char* src;
+    unsigned char* dst;
+    uint32_t len;
+    while (next_chunk(a, cons, &src, &dst, &len)) {
+      const int s = (int)(done % kGatStages);
+      if (!mbar_wait(&full[s], (uint32_t)((done / kGatStages) & 1))) {
+        ok = false;
+        break;
+      }
+      bulk_store(dst, smem + (size_t)s * kGatChunk, len);
+      bulk_commit();
+      ++done;
+      // the next load goes to the buffer of chunk done - 2, whose store is not the newest
+      bulk_wait_read_all_but_one();
+      issue();
+    }
+    // a wait that gave up: let every load still in flight land before the CTA exits
+    for (long long k = done; k < issued; ++k)
+      mbar_wait(&full[(int)(k % kGatStages)], (uint32_t)((k / kGatStages) & 1));
     bulk_wait_all();
     if (!ok && a.status) atomicExch(a.status, kStatusGatherWait);
+  } else if (tid >= 32) {
+    const int warp = tid / 32 - 1, lane = tid % 32, warps = kGatThreads / 32 - 1;
+    int seg = 0;
+    long long k = 0;
+    for (long long t = blockIdx.x; t < a.tiles; t += gridDim.x, ++k) {
+      const AlTile m = al_tile(a, seg, t);
+      if (k % warps != warp) continue;
+      if (m.body == 0) {  // no bulk part: the whole tile element by element
+        for (long long i = lane; i < m.n; i += 32) m.dst[i] = m.src[i];
+        continue;
+      }
+      if (lane < m.head) m.dst[lane] = m.src[lane];
+      const long long t0 = m.head + m.body;
+      if (t0 + lane < m.n) m.dst[t0 + lane] = m.src[t0 + lane];
+    }
   }
 }
 

@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include <cstddef>
+#include <cstring>
 
 #include "internal.h"
 
@@ -34,14 +35,15 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once per device.
-cudaError_t scratch_address(void** out) {
+// Device address of the scratch array on the current device, looked up once per device
+// (or, with lookup == false, only if it was looked up before; else *out = nullptr).
+cudaError_t scratch_address(void** out, bool lookup = true) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_addr[dev]) {
+  if (!g_addr[dev] && lookup) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
@@ -166,5 +168,36 @@ extern "C" int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid,
 
   e = cudaMemcpyAsync(step_counter, &st->step, sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return bad(ZERO_ECUDA, "step counter copy failed");
+  return ZERO_OK;
+}
+
+extern "C" int zero_noalloc_step_result(void* stream, zero_step_info* out) {
+  using namespace zero;
+  set_error(ZERO_OK, "");
+  if (!out) return set_error(ZERO_EINVAL, "out is NULL");
+  void* base = nullptr;
+  cudaError_t e = scratch_address(&base, false);
+  if (e != cudaSuccess) return set_error(ZERO_ECUDA, "cudaGetDevice failed");
+  if (!base)
+    return set_error(ZERO_EUNBOUND, "no allocation-free step has run on the current device");
+  const DevScratch* st = static_cast<const DevScratch*>(base);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevScalars sc;  // pageable: the copy completes before cudaMemcpyAsync returns
+  e = cudaMemcpyAsync(&sc, &st->sc, sizeof sc, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(ZERO_ECUDA, "copy of the step result failed");
+  memset(out, 0, sizeof *out);
+  out->overflow = sc.overflow;
+  out->skipped = sc.skipped;
+  out->status = sc.status;
+  out->step = sc.step;
+  out->global_norm = sc.norm;
+  out->sum_sq = sc.ss;
+  out->clip_coef = sc.clip_coef;
+  out->scale = sc.s;
+  out->bc1 = sc.bc1;
+  out->bc2 = sc.bc2;
+  out->loss_scale = sc.loss_scale;
+  if (sc.status != 0) return set_error(ZERO_EDEVICE, "the allocation-free step reported a device failure");
   return ZERO_OK;
 }

@@ -72,6 +72,10 @@ struct zero_plan {
   // and joined before the caller's stream goes on
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // second stream of the layer-by-layer gather (zero_gather_layers_events): every other
+  // layer's copy runs there, so that it starts on the SMs the previous layer leaves
+  cudaStream_t gside = nullptr;
+  cudaEvent_t gev_fork = nullptr, gev_join = nullptr;
   bool stepped = false;
 
   bool scaler_on = false;  // host mirror of the device scaler's on/off switch
@@ -183,24 +187,30 @@ int ensure_scratch(zero_plan* p, int dev) {
   }
   // the second stream for the next step's t-only scalars, made here (outside any graph
   // capture the caller may start later)
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaStream_t side = nullptr, gside = nullptr;
+  cudaEvent_t ev[4] = {};
   e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&gside, cudaStreamNonBlocking);
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+    e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
   if (e != cudaSuccess) {
-    if (ev_fork) cudaEventDestroy(ev_fork);
+    for (cudaEvent_t x : ev)
+      if (x) cudaEventDestroy(x);
+    if (gside) cudaStreamDestroy(gside);
     if (side) cudaStreamDestroy(side);
     cudaFreeHost(hs);
     cudaFree(sc);
-    return cuda_fail(e, "second stream");
+    return cuda_fail(e, "second streams");
   }
   p->scratch = sc;
   p->host_sc = hs;
   p->device = dev;
   p->side = side;
-  p->ev_fork = ev_fork;
-  p->ev_join = ev_join;
+  p->ev_fork = ev[0];
+  p->ev_join = ev[1];
+  p->gside = gside;
+  p->gev_fork = ev[2];
+  p->gev_join = ev[3];
   return ZERO_OK;
 }
 
@@ -306,6 +316,92 @@ int do_update(zero_plan* p, cudaStream_t s) {
   return ZERO_OK;
 }
 
+// Arguments of a gather: checked in full before anything is enqueued. Allocates the
+// plan's device scratch (which holds the gather's status word) on first use.
+int check_gather(zero_plan* p, const int64_t* offs, int32_t n_layers, const void* const* shards,
+                 void* const* dst) {
+  if (!p) return fail(ZERO_EINVAL, "plan is NULL");
+  if (!offs || !shards || !dst) return fail(ZERO_EINVAL, "NULL array argument");
+  if (n_layers < 1) return fail(ZERO_EINVAL, "n_layers must be >= 1");
+  if (offs[0] < 0) return fail(ZERO_EINVAL, "layer_offsets[0] must be >= 0");
+  for (int l = 0; l < n_layers; ++l) {
+    if (offs[l + 1] < offs[l]) return fail(ZERO_EINVAL, "layer_offsets must be non-decreasing");
+    if (offs[l + 1] > offs[l]) {
+      if (!dst[l]) return fail(ZERO_EINVAL, "layer_dst[%d] is NULL", l);
+      if (reinterpret_cast<uintptr_t>(dst[l]) & 1u)
+        return fail(ZERO_EALIGN, "layer_dst[%d] is not 2-byte aligned", l);
+    }
+  }
+  if (offs[n_layers] > p->n)
+    return fail(ZERO_EINVAL, "layer_offsets[%d] = %lld exceeds n_params = %lld", n_layers,
+                (long long)offs[n_layers], (long long)p->n);
+  for (int r = 0; r < p->nd; ++r) {
+    if (!shards[r]) return fail(ZERO_EINVAL, "shard_ptrs[%d] is NULL", r);
+    if (reinterpret_cast<uintptr_t>(shards[r]) & 1u)
+      return fail(ZERO_EALIGN, "shard_ptrs[%d] is not 2-byte aligned", r);
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->device >= 0 && dev != p->device)
+    return fail(ZERO_EINVAL, "current device %d differs from the plan's device %d", dev, p->device);
+  return ensure_scratch(p, dev);
+}
+
+// The two segment tables of a gather launch: source and destination equal modulo 16 bytes
+// (t[0], k_gather), or not (t[1], k_gather_realign); tiles are numbered per table.
+struct GatherTables {
+  zero::GatherLaunch t[2];
+  explicit GatherTables(zero_plan* p) {
+    for (int k = 0; k < 2; ++k) {
+      t[k].nseg = 0;
+      t[k].tiles = 0;
+      t[k].grid = 0;
+      t[k].status = &p->scratch->gather_status;
+      t[k].realign = k;
+    }
+  }
+};
+
+int flush_gather(zero_plan* p, zero::GatherLaunch& gl, cudaStream_t s) {
+  if (gl.nseg == 0) return ZERO_OK;
+  EventPair ev;
+  prof_begin(p, s, &ev);
+  cudaError_t e = zero::launch_gather(gl, s);
+  prof_end(p, s, &ev, 3);
+  gl.nseg = 0;
+  gl.tiles = 0;
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  return ZERO_OK;
+}
+
+// Cut layer l at shard boundaries into copy segments, each into the table of its alignment
+// class; a full table is launched on s first.
+int plan_layer(zero_plan* p, const int64_t* offs, int l, const void* const* shards,
+               void* const* dst, GatherTables& gt, cudaStream_t s) {
+  const int64_t a = offs[l], b = offs[l + 1];
+  for (int64_t r = a / p->s; a < b && r * p->s < b; ++r) {
+    const int64_t lo = std::max(a, r * p->s), hi = std::min(b, (r + 1) * p->s);
+    if (hi <= lo) continue;
+    const uint16_t* src = static_cast<const uint16_t*>(shards[r]) + (lo - r * p->s);
+    uint16_t* dptr = static_cast<uint16_t*>(dst[l]) + (lo - a);
+    const int k =
+        ((reinterpret_cast<uintptr_t>(src) - reinterpret_cast<uintptr_t>(dptr)) & 15u) ? 1 : 0;
+    zero::GatherLaunch& gl = gt.t[k];
+    if (gl.nseg == zero::kGatherSegs) {
+      int rc = flush_gather(p, gl, s);
+      if (rc) return rc;
+    }
+    zero::GatherSeg& sg = gl.seg[gl.nseg++];
+    sg.src = src;
+    sg.dst = dptr;
+    sg.len = hi - lo;
+    sg.tile_begin = gl.tiles;
+    gl.tiles += (sg.len + zero::kGatherTile - 1) / zero::kGatherTile;
+  }
+  return ZERO_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -360,6 +456,9 @@ void zero_plan_destroy(zero_plan* p) {
   if (p->side) cudaStreamDestroy(p->side);
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->ev_join) cudaEventDestroy(p->ev_join);
+  if (p->gside) cudaStreamDestroy(p->gside);
+  if (p->gev_fork) cudaEventDestroy(p->gev_fork);
+  if (p->gev_join) cudaEventDestroy(p->gev_join);
   if (p->scratch) cudaFree(p->scratch);
   if (p->host_sc) cudaFreeHost(p->host_sc);
   if (has_dev && prev != p->device) cudaSetDevice(prev);
@@ -527,82 +626,52 @@ int zero_step_result(zero_plan* p, zero_step_info* out) {
 int zero_gather_layers(zero_plan* p, const int64_t* offs, int32_t n_layers,
                        const void* const* shards, void* const* dst, void* stream) {
   g_error.clear();
-  if (!p) return fail(ZERO_EINVAL, "plan is NULL");
-  if (!offs || !shards || !dst) return fail(ZERO_EINVAL, "NULL array argument");
-  if (n_layers < 1) return fail(ZERO_EINVAL, "n_layers must be >= 1");
-  if (offs[0] < 0) return fail(ZERO_EINVAL, "layer_offsets[0] must be >= 0");
-  for (int l = 0; l < n_layers; ++l) {
-    if (offs[l + 1] < offs[l]) return fail(ZERO_EINVAL, "layer_offsets must be non-decreasing");
-    if (offs[l + 1] > offs[l]) {
-      if (!dst[l]) return fail(ZERO_EINVAL, "layer_dst[%d] is NULL", l);
-      if (reinterpret_cast<uintptr_t>(dst[l]) & 1u)
-        return fail(ZERO_EALIGN, "layer_dst[%d] is not 2-byte aligned", l);
-    }
-  }
-  if (offs[n_layers] > p->n)
-    return fail(ZERO_EINVAL, "layer_offsets[%d] = %lld exceeds n_params = %lld", n_layers,
-                (long long)offs[n_layers], (long long)p->n);
-  for (int r = 0; r < p->nd; ++r) {
-    if (!shards[r]) return fail(ZERO_EINVAL, "shard_ptrs[%d] is NULL", r);
-    if (reinterpret_cast<uintptr_t>(shards[r]) & 1u)
-      return fail(ZERO_EALIGN, "shard_ptrs[%d] is not 2-byte aligned", r);
-  }
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (p->device >= 0 && dev != p->device)
-    return fail(ZERO_EINVAL, "current device %d differs from the plan's device %d", dev, p->device);
-  int rc0 = ensure_scratch(p, dev);  // holds the gather's status word
-  if (rc0) return rc0;
-
-  // Cut each layer at shard boundaries; a segment goes to the table of its alignment class
-  // (source and destination equal modulo 16 bytes, or not); tiles are numbered in order.
+  int rc = check_gather(p, offs, n_layers, shards, dst);
+  if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  zero::GatherLaunch tables[2];
-  for (int k = 0; k < 2; ++k) {
-    tables[k].nseg = 0;
-    tables[k].tiles = 0;
-    tables[k].grid = 0;
-    tables[k].status = &p->scratch->gather_status;
-    tables[k].realign = k;
-  }
-  auto flush = [&](zero::GatherLaunch& gl) -> int {
-    if (gl.nseg == 0) return ZERO_OK;
-    EventPair ev;
-    prof_begin(p, s, &ev);
-    cudaError_t le = zero::launch_gather(gl, s);
-    prof_end(p, s, &ev, 3);
-    gl.nseg = 0;
-    gl.tiles = 0;
-    if (le != cudaSuccess) return cuda_fail(le, "gather launch");
-    return ZERO_OK;
-  };
-  for (int l = 0; l < n_layers; ++l) {
-    const int64_t a = offs[l], b = offs[l + 1];
-    if (a == b) continue;
-    for (int64_t r = a / p->s; r * p->s < b; ++r) {
-      const int64_t lo = std::max(a, r * p->s), hi = std::min(b, (r + 1) * p->s);
-      if (hi <= lo) continue;
-      const uint16_t* src = static_cast<const uint16_t*>(shards[r]) + (lo - r * p->s);
-      uint16_t* dptr = static_cast<uint16_t*>(dst[l]) + (lo - a);
-      const int k = ((reinterpret_cast<uintptr_t>(src) - reinterpret_cast<uintptr_t>(dptr)) & 15u) ? 1 : 0;
-      zero::GatherLaunch& gl = tables[k];
-      if (gl.nseg == zero::kGatherSegs) {
-        int rc = flush(gl);
-        if (rc) return rc;
-      }
-      zero::GatherSeg& sg = gl.seg[gl.nseg++];
-      sg.src = src;
-      sg.dst = dptr;
-      sg.len = hi - lo;
-      sg.tile_begin = gl.tiles;
-      gl.tiles += (sg.len + zero::kGatherTile - 1) / zero::kGatherTile;
+  GatherTables gt(p);
+  for (int l = 0; l < n_layers && !rc; ++l) rc = plan_layer(p, offs, l, shards, dst, gt, s);
+  if (!rc) rc = flush_gather(p, gt.t[0], s);
+  if (!rc) rc = flush_gather(p, gt.t[1], s);
+  if (!rc) p->gather_stream = s;
+  return rc;
+}
+
+int zero_gather_layers_events(zero_plan* p, const int64_t* offs, int32_t n_layers,
+                              const void* const* shards, void* const* dst,
+                              void* const* layer_done, void* stream) {
+  g_error.clear();
+  if (!layer_done) return fail(ZERO_EINVAL, "layer_done is NULL");
+  int rc = check_gather(p, offs, n_layers, shards, dst);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // layers 0, 2, 4, ... on the caller's stream, 1, 3, 5, ... on the plan's second gather
+  // stream, which starts after the work already on `stream` and is joined back into it
+  // at the end: consecutive layers overlap, so the next layer's CTAs take the SMs the
+  // previous layer's last CTAs leave, and each layer's event marks that layer alone
+  cudaError_t e = cudaEventRecord(p->gev_fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->gside, p->gev_fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "gather fork");
+  GatherTables gt(p);
+  for (int l = 0; l < n_layers && !rc; ++l) {
+    cudaStream_t sl = (l & 1) ? p->gside : s;
+    rc = plan_layer(p, offs, l, shards, dst, gt, sl);
+    if (!rc) rc = flush_gather(p, gt.t[0], sl);
+    if (!rc) rc = flush_gather(p, gt.t[1], sl);
+    if (!rc && layer_done[l]) {
+      e = cudaEventRecord(static_cast<cudaEvent_t>(layer_done[l]), sl);
+      if (e != cudaSuccess)
+        rc = fail(ZERO_ECUDA, "cudaEventRecord(layer_done[%d]): %s (%d)", l,
+                  cudaGetErrorString(e), (int)e);
     }
   }
-  rc0 = flush(tables[0]);
-  if (!rc0) rc0 = flush(tables[1]);
-  if (!rc0) p->gather_stream = s;
-  return rc0;
+  // join even after an error, so that the caller's stream still orders after the work
+  // already enqueued
+  e = cudaEventRecord(p->gev_join, p->gside);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, p->gev_join, 0);
+  if (!rc && e != cudaSuccess) rc = cuda_fail(e, "gather join");
+  if (!rc) p->gather_stream = s;
+  return rc;
 }
 
 int zero_gather_status(zero_plan* p, int32_t* status) {

@@ -163,3 +163,20 @@ def make_shards(w: Workload, shard0, device="cuda") -> list:
         fill(t, key(w, SHARD16, 0, r), w.shard_sigma, start=r * s, n_valid=w.n)
         shards.append(t)
     return shards
+
+
+def span_shards(w: Workload, span16, device="cuda") -> list:
+    """The nd fp16 shards for the gather after a step over the span [r0, r1): the span's
+    own shards are slices of ``span16`` (the step's fp16 output, (r1 - r0) * S elements),
+    the other ranks' are seeded N(0, shard_sigma) values of their own flat indices."""
+    import torch
+    _, s = w.layout()
+    shards = []
+    for r in range(w.nd):
+        if w.r0 <= r < w.r1:
+            shards.append(span16[(r - w.r0) * s:(r - w.r0 + 1) * s])
+            continue
+        t = torch.empty(s, dtype=torch.float16, device=device)
+        fill(t, key(w, SHARD16, 0, r), w.shard_sigma, start=r * s, n_valid=w.n)
+        shards.append(t)
+    return shards

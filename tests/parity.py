@@ -1,10 +1,14 @@
 """Parity harness: drive the GPU library and the CPU oracle on the same seeded inputs.
 
 Expected values come only from the oracle, fed with the input bytes (gradients, initial
-state) that the seeded generator wrote. Two modes:
+state) that the seeded generator wrote. Three modes:
 
 * full: every element of every output is compared (sizes the oracle finishes in
   seconds);
+* full_parallel: the same comparison of every element, with the oracle's step run over
+  slices of the span on all host threads (bench.PartitionedOracle, bit-identical to one
+  oracle step: the slices' integer statistics are added exactly before the scalars are
+  taken), for full-size workloads whose inputs and state fit in host memory;
 * sampled: the oracle streams all gradients through its reduce and exact sum of squares
   (the global norm and overflow flag need the whole span), then follows a sample of
   elements through every step with those scalars.
@@ -90,6 +94,25 @@ def assert_info_matches(info: z.zero_step_info, sc: oracle.Scalars):
     assert np.float32(info.bc2) == np.float32(sc.bc2)
 
 
+def assert_state_full(name, got, exp, chunk=1 << 24) -> bool:
+    """Every element of a full-size fp32 state array: True if bit-identical, else checked
+    chunk by chunk at the 1e-6 relative bar (and False)."""
+    if np.array_equal(got.view(np.uint32), exp.view(np.uint32)):
+        return True
+    for a in range(0, len(got), chunk):
+        assert_state_close(name, got[a:a + chunk], exp[a:a + chunk],
+                           np.arange(a, min(a + chunk, len(got))))
+    return False
+
+
+def assert_p16_full(got, exp, chunk=1 << 24) -> bool:
+    if np.array_equal(got, exp):
+        return True
+    for a in range(0, len(got), chunk):
+        assert_p16_close(got[a:a + chunk], exp[a:a + chunk], np.arange(a, min(a + chunk, len(got))))
+    return False
+
+
 def pytest_approx(x, rel):
     import pytest
     return pytest.approx(x, rel=rel)
@@ -161,7 +184,7 @@ def take(t: torch.Tensor, idx: np.ndarray) -> torch.Tensor:
 class Runner:
     """One workload on the device through the C ABI, followed by the oracle."""
     w: wl.Workload
-    mode: str = "full"                      # or "sampled"
+    mode: str = "full"                      # or "full_parallel", "sampled"
     steps: int | None = None
     results: list = field(default_factory=list)
     exact: bool = True
@@ -176,8 +199,11 @@ class Runner:
         torch.cuda.synchronize()
         plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
         z.zero_plan_bind(plan, w.r0, w.r1, master, m, v, p16, ws, 0)
-        if self.mode == "full":
+        if self.mode in ("full", "full_parallel"):
             om, omm, ov, op = f32(master).copy(), f32(m).copy(), f32(v).copy(), h16(p16).copy()
+            if self.mode == "full_parallel":
+                import bench
+                par = bench.PartitionedOracle(n_valid, THREADS)
         else:
             idx = sample_indices(n_valid, s)
             smp = Sample(idx, f32(take(master, idx)).copy(), f32(take(m, idx)).copy(),
@@ -214,6 +240,28 @@ class Runner:
                                np.array_equal(gmm.view(np.uint32), omm.view(np.uint32)) and
                                np.array_equal(gv.view(np.uint32), ov.view(np.uint32)) and
                                np.array_equal(gp, op))
+            elif self.mode == "full_parallel":
+                nv = n_valid
+                host = [h16(g)[:nv] for g in grads]
+                sc = par.step(host, om[:nv], omm[:nv], ov[:nv], op[:nv], w.loss_scale, w.clip,
+                              hp, t, keep_sums=True)
+                del host
+                assert_info_matches(info, sc)
+                if not sc.skipped and not one_launch:
+                    gws = f32(ws)
+                    for sl, gs in zip(par.slices, par.sums):
+                        assert np.array_equal(gws[sl].view(np.uint32), gs.view(np.uint32))
+                    del gws
+                for name, got, exp in (("master", master, om), ("exp_avg", m, omm),
+                                       ("exp_avg_sq", v, ov)):
+                    g_ = f32(got)
+                    self.exact &= assert_state_full(name, g_[:nv], exp[:nv])
+                    assert not g_[nv:].any()  # padding is never touched
+                    del g_
+                gp = h16(p16)
+                self.exact &= assert_p16_full(gp[:nv], op[:nv])
+                assert not gp[nv:].any()
+                del gp
             else:
                 bad, ss = oracle_span_stats(grads, n_valid)
                 sc = oracle.scalars(bad, ss, w.loss_scale, w.clip, hp, t)
@@ -234,6 +282,8 @@ class Runner:
                                np.array_equal(gp, smp.p16))
             t = sc.step
             self.results.append(info.as_dict())
+        if self.mode == "full_parallel":
+            par.close()
         self.state = (master, m, v, p16, ws)
         self.plan = plan
         return self

@@ -123,6 +123,15 @@ def test_gather_rejects_bad_arguments():
         expect(z.ZERO_EINVAL, z.zero_gather_layers, p, [0, 50, 100], shards[:3] + [0], dst, 0)
         expect(z.ZERO_EALIGN, z.zero_gather_layers, p, [0, 50, 100], shards[:3] + [shards[3] + 1],
                dst, 0)
+        # the layer-by-layer form: the same checks, plus the event array itself
+        ev = [0x70000, 0]
+        expect(z.ZERO_EINVAL, z.zero_gather_layers_events, p, [0, 60, 50], shards, dst, ev, 0)
+        expect(z.ZERO_EALIGN, z.zero_gather_layers_events, p, [0, 50, 100], shards,
+               [0x40001, 0x50000], ev, 0)
+        expect(z.ZERO_EINVAL, z.zero_gather_layers_events, p, [0, 50, 100], shards, dst, [0], 0)
+        offs = (z._I64 * 3)(0, 50, 100)
+        rc = z._lib.zero_gather_layers_events(p, offs, 2, z._ptrs(shards), z._ptrs(dst), None, 0)
+        assert rc == z.ZERO_EINVAL and "layer_done" in z.zero_last_error()
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

@@ -39,15 +39,41 @@ def check_cpu_baseline(c):
     assert isinstance(c["unit"], str) and isinstance(c["sample"], str)
 
 
+def check_roofline(r):
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    assert bench.DEFAULT_WORKLOAD == "zero3_13b_rank0_nd64"
+
+
 def test_reference_arm_line():
     d = run(["--impl", "reference", "--workload", "zero2_tiny_1m_nd4", "--steps", "2",
-             "--warmup", "3"])
+             "--warmup", "3", "--cpu-seconds", "0.5"])
     check_common(d)
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
     check_cpu_baseline(d["cpu_baseline"])
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    check_cpu_baseline(d["gather"]["cpu_baseline"])
+    # the oracle arm names the workload exactly as the GPU arm does
+    from synth import workloads as wl
+    assert d["config"] == bench.config_of(wl.WORKLOADS["zero2_tiny_1m_nd4"], 1)
+    assert d["scaling"] == "strong"
+
+
+def test_process_spans():
+    from synth import workloads as wl
+    w5 = wl.WORKLOADS["zero3_13b_rank0_nd64"]
+    spans = [bench.process_span(w5, 4, g) for g in range(4)]
+    assert [(w.r0, w.r1, k) for w, k in spans] == [(g, g + 1, "weak") for g in range(4)]
+    assert bench.job_params(w5, 4) == 4 * w5.span()[2]
+    w2 = wl.WORKLOADS["gpt2_small_flat_nd8"]
+    spans = [bench.process_span(w2, 2, g) for g in range(2)]
+    assert [(w.r0, w.r1, k) for w, k in spans] == [(0, 4, "strong"), (4, 8, "strong")]
+    assert bench.job_params(w2, 2) == w2.n
 
 
 @pytest.mark.gpu
@@ -60,14 +86,26 @@ def test_step_line():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 2 * 1048576
     assert e["d2h_bytes_per_step"] > 0 and set(e["by_mode"]) == {"copy", "copy_overlap",
                                                                   "zero_copy"}
+    assert e["value"] == max(e["by_mode"].values())
+    p = e["with_params_to_host"]
+    assert p["value"] > 0 and p["d2h_bytes_per_step"] == e["d2h_bytes_per_step"] + 2 * 1048576
     assert d["gpu_launches"] >= 20  # one launch per step for this small span, else two or three
-    r = d["roofline"]
-    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
-    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    check_roofline(d["roofline"])
     check_cpu_baseline(d["cpu_baseline"])
     c = d["clocks"]
     assert "sm_mhz" in c and "sm_max_mhz" in c and isinstance(c["reasons"], list)
     assert d["last_step"]["skipped"] == 0
+    # the gather of the step's output (one full-buffer layer here) in the same line
+    g = d["gather"]
+    assert g["value"] > 0 and g["layers"] == 1 and g["params_per_call"] == 1048576
+    assert g["gpu_launches"] == 20
+    check_roofline(g["roofline"])
+    check_cpu_baseline(g["cpu_baseline"])
+    assert d["hot_path"]["ms_per_pass"] > 0
+    # both arms name the workload identically
+    ref = run(["--impl", "reference", "--workload", "zero2_tiny_1m_nd4", "--steps", "2",
+               "--warmup", "3", "--cpu-seconds", "0"])
+    assert ref["config"] == d["config"] and ref["scaling"] == d["scaling"]
 
 
 @pytest.mark.gpu
@@ -96,4 +134,5 @@ def test_gather_prefetch_line():
     layers = d["config"]["layers"]
     assert d["gpu_launches"] == 3 * layers
     ready = d["prefetch"]["layer_ready_ms"]
-    assert len(ready) == layers and ready == sorted(ready) and ready[0] < ready[-1]
+    # consecutive layers run on two streams, so their events need not complete in order
+    assert len(ready) == layers and min(ready) > 0 and ready[0] < max(ready)

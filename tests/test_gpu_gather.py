@@ -111,3 +111,46 @@ def test_prefetch_layers_with_per_layer_events():
         assert np.array_equal(h16(dst[l]), exp[l])
         assert sums[l].item() == int(exp[l].view(np.int16).astype(np.int64).sum())
     plan.close()
+
+
+def test_gather_layers_events_misaligned_layers_and_missing_events():
+    # odd layer boundaries (both the bulk-copy and the realigning kernel run), a layer
+    # without an event, an empty layer; each layer is read on another stream right after
+    # its own event, and work enqueued on the call's stream afterwards sees every layer
+    n, nd = 3_000_017, 8
+    np_, s = oracle.partition(n, nd, 8)
+    g = torch.Generator(device="cuda").manual_seed(4)
+    shards = [torch.randint(-32768, 32767, (s,), dtype=torch.int16, device="cuda", generator=g)
+              for _ in range(nd)]
+    offs = [0, 8, 400_003, 400_003, 1_200_000, 1_999_999, 2_400_000, n]
+    dst = [torch.full((max(1, offs[l + 1] - offs[l]),), -1, dtype=torch.int16, device="cuda")
+           for l in range(len(offs) - 1)]
+    plan = z.zero_plan_create(n, nd, 3, 8, HP)
+    producer, consumer = torch.cuda.Stream(), torch.cuda.Stream()
+    events = z.make_layer_events(len(offs) - 1)
+    events[3] = None
+    torch.cuda.synchronize()
+    z.zero_profile_enable(plan, True)
+    z.zero_gather_layers_events(plan, offs, shards, dst, events, producer)
+    sums = {}
+    for l, ev in enumerate(events):
+        if ev is None:
+            continue
+        consumer.wait_event(ev)
+        with torch.cuda.stream(consumer):
+            sums[l] = dst[l][:offs[l + 1] - offs[l]].to(torch.int64).sum()
+    with torch.cuda.stream(producer):  # after the call on its own stream: all layers
+        total = torch.stack([d[:offs[l + 1] - offs[l]].to(torch.int64).sum()
+                             for l, d in enumerate(dst)]).sum()
+    torch.cuda.synchronize()
+    assert z.zero_gather_status(plan) == 0
+    launches = z.zero_profile_read(plan)[1][z.PROF_GATHER]
+    assert launches >= len(offs) - 2  # one launch (or two) per non-empty layer
+    exp = oracle.gather([h16(x) for x in shards], s, offs)
+    for l in range(len(offs) - 1):
+        got = h16(dst[l])[:offs[l + 1] - offs[l]]
+        assert np.array_equal(got, exp[l]), l
+        if l in sums:
+            assert sums[l].item() == int(exp[l].view(np.int16).astype(np.int64).sum()), l
+    assert total.item() == sum(int(e.view(np.int16).astype(np.int64).sum()) for e in exp)
+    plan.close()

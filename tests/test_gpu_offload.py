@@ -16,10 +16,15 @@ from parity import assert_info_matches, f32, h16, hyper
 pytestmark = pytest.mark.gpu
 
 
-def test_step_with_state_in_pinned_host_memory():
-    w = wl.Workload("offload", cfg=500, n=1_000_003, nd=8, align=8, stage=2, r0=0, r1=8,
+@pytest.mark.parametrize("n", [1_000_003, 6_000_001])
+def test_step_with_state_in_pinned_host_memory(n):
+    # 1,000,003 parameters run the one-launch step; 6,000,001 (above its limit on a
+    # 152-SM part) run the reduce and the bulk-copy update kernel, whose TMA loads and
+    # stores then address pinned host memory. The second step carries a +inf in rank 3
+    # and must leave the host-resident state untouched.
+    w = wl.Workload("offload", cfg=500, n=n, nd=8, align=8, stage=2, r0=0, r1=8,
                     loss_scale=65536.0, grad_sigma=1e-3, clip=1.0, steps=3, m_sigma=1e-3,
-                    v_sigma=1e-6)
+                    v_sigma=1e-6, inject=((1, 3, wl.POS_INF, n // 3),))
     first, n_span, n_valid = w.span()
     dev_state = wl.make_state(w)
     host_state = [t.cpu().pin_memory() for t in dev_state[:4]]
@@ -27,6 +32,9 @@ def test_step_with_state_in_pinned_host_memory():
                        f32(dev_state[2]).copy(), h16(dev_state[3]).copy())
     plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
     z.zero_plan_bind(plan, 0, w.nd, *host_state, dev_state[4], 0)  # workspace stays in HBM
+    z.zero_profile_enable(plan, True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    one_launch = n_span // 8 <= 3072 * sms
     t = 0
     for step in range(w.steps):
         grads = wl.make_grads(w, step)
@@ -35,12 +43,18 @@ def test_step_with_state_in_pinned_host_memory():
         sc = oracle.step([h16(g) for g in grads], om, omm, ov, op, w.loss_scale, w.clip,
                          hyper(w), t, n_valid=n_valid)
         assert_info_matches(info, sc)
+        assert sc.skipped == (step == 1)
         t = sc.step
-    torch.cuda.synchronize()
-    assert np.array_equal(host_state[0].numpy().view(np.uint32), om.view(np.uint32))
-    assert np.array_equal(host_state[1].numpy().view(np.uint32), omm.view(np.uint32))
-    assert np.array_equal(host_state[2].numpy().view(np.uint32), ov.view(np.uint32))
-    assert np.array_equal(host_state[3].view(torch.int16).numpy().view(np.uint16), op)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_state[0].numpy().view(np.uint32), om.view(np.uint32))
+        assert np.array_equal(host_state[1].numpy().view(np.uint32), omm.view(np.uint32))
+        assert np.array_equal(host_state[2].numpy().view(np.uint32), ov.view(np.uint32))
+        assert np.array_equal(host_state[3].view(torch.int16).numpy().view(np.uint16), op)
+    launches = z.zero_profile_read(plan)[1]
+    if one_launch:
+        assert launches[z.PROF_STEP] == w.steps and launches[z.PROF_UPDATE] == 0
+    else:
+        assert launches[z.PROF_UPDATE] == w.steps and launches[z.PROF_STEP] == 0
     plan.close()
 
 
