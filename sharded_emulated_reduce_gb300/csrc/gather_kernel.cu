@@ -61,34 +61,13 @@ __device__ __forceinline__ AlTile al_tile(const GatherLaunch& a, int& seg, long 
   return m;
 }
 
-// Walks this CTA's bulk-copy chunks in order: its tiles blockIdx.x, + gridDim.x, ...,
-// each tile's body cut into chunks of at most kGatChunk bytes (multiples of 16 bytes,
-// 16-byte-aligned addresses).
-struct ChunkIt {
-  long long t;    // current tile
-  long long off;  // byte offset of the next chunk in the tile's body
-  int seg;
+// A tile body in thread 0's queue of claimed tiles.
+struct Body {
+  const unsigned char* src;
+  unsigned char* dst;
+  long long bytes;  // a positive multiple of 16; both addresses 16-byte aligned
 };
-
-__device__ __forceinline__ bool next_chunk(const GatherLaunch& a, ChunkIt& it,
-                                           const unsigned char** src, unsigned char** dst,
-                                           uint32_t* len) {
-  while (it.t < a.tiles) {
-    const AlTile m = al_tile(a, it.seg, it.t);
-    const long long bytes = 2 * m.body;
-    if (it.off < bytes) {
-      const long long left = bytes - it.off;
-      *len = (uint32_t)(left < (long long)kGatChunk ? left : (long long)kGatChunk);
-      *src = reinterpret_cast<const unsigned char*>(m.src + m.head) + it.off;
-      *dst = reinterpret_cast<unsigned char*>(m.dst + m.head) + it.off;
-      it.off += *len;
-      return true;
-    }
-    it.t += gridDim.x;
-    it.off = 0;
-  }
-  return false;
-}
+constexpr int kGatQueue = kGatStages + 2;  // claimed tiles held at once (see k_gather)
 
 // Bytes [D, D+16) of the 32-byte concatenation lo|hi, for an even D in 0..14 (little
 // endian: lo.x holds bytes 0..3).
@@ -160,54 +139,101 @@ __device__ __forceinline__ MisTile mis_tile(const GatherLaunch& L, int& seg, lon
   return m;
 }
 
-// Thread 0 streams all of this CTA's chunks through one ring of kGatStages buffers:
-// kGatStages - 1 bulk loads stay in flight, each landed chunk leaves by a bulk store, and
-// a buffer is refilled once the store before the newest one has finished reading it. The
-// ring does not drain between tiles. Warps 1.. copy the tiles' unaligned edge elements
-// meanwhile (disjoint bytes from the bulk stores). A CTA visits its tiles in increasing
-// order, so the segment that holds a tile is found by advancing a running index.
+// Thread 0 claims tiles one at a time from the launch's counter (an atomic add, so a CTA
+// on a slower SM simply claims fewer and every CTA finishes at about the same time) and
+// streams their 16-byte-aligned bodies, cut into chunks of at most kGatChunk bytes,
+// through one ring of kGatStages buffers: kGatStages - 1 bulk loads stay in flight, each
+// landed chunk leaves by a bulk store, and a buffer is refilled once the store before the
+// newest one has finished reading it. The ring does not drain between tiles. Tiles
+// without a body are not queued, so the queue never holds more than kGatStages tiles
+// (the consumer's and one per chunk in flight). The other warps copy the unaligned edge
+// elements of every tile of the launch, split statically over the CTAs (disjoint bytes
+// from the bulk stores). The last CTA to finish resets the counter for the next launch.
 __global__ void __launch_bounds__(kGatThreads, 1) k_gather(const __grid_constant__ GatherLaunch a) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kGatStages * kGatChunk);
   const int tid = threadIdx.x;
-  bool ok = true;
   if (tid == 0) {
+    bool ok = true;
     for (int s = 0; s < kGatStages; ++s) mbar_init(&full[s], 1);
     mbar_fence_init();
-    ChunkIt prod{(long long)blockIdx.x, 0, 0}, cons{(long long)blockIdx.x, 0, 0};
-    long long issued = 0, done = 0;
-    auto issue = [&]() {
-      const unsigned char* src;
-      unsigned char* dst;
-      uint32_t len;
-      if (!next_chunk(a, prod, &src, &dst, &len)) return;
-      const int s = (int)(issued % kGatStages);
-      mbar_expect_tx(&full[s], len);
-      bulk_load(smem + (size_t)s * kGatChunk, src, len, &full[s]);
-      ++issued;
+    Body q[kGatQueue];
+    long long q_head = 0, q_tail = 0;  // the consumer's tile is q[q_head], the next free q[q_tail]
+    long long p_idx = 0, p_off = 0;    // the producer's tile and byte offset in its body
+    long long c_off = 0;               // the consumer's byte offset in q[q_head]
+    int claim_seg = 0;
+    bool claims_done = false;
+    // one more tile with a body into the queue; false when none is left (or no room)
+    auto claim = [&]() -> bool {
+      while (!claims_done && q_tail - q_head < kGatQueue) {
+        const long long t = (long long)atomicAdd(a.sched, 1ull);
+        if (t >= a.tiles) {
+          claims_done = true;
+          break;
+        }
+        const AlTile m = al_tile(a, claim_seg, t);
+        if (m.body == 0) continue;  // edges only: the other warps copy it
+        Body& b = q[q_tail % kGatQueue];
+        b.src = reinterpret_cast<const unsigned char*>(m.src + m.head);
+        b.dst = reinterpret_cast<unsigned char*>(m.dst + m.head);
+        b.bytes = 2 * m.body;
+        ++q_tail;
+        return true;
+      }
+      return false;
     };
-    for (int k = 0; k < kGatStages - 1; ++k) issue();
-    const unsigned char* src;
-    unsigned char* dst;
-    uint32_t len;
-    while (next_chunk(a, cons, &src, &dst, &len)) {
+    long long issued = 0, done = 0;
+    // issue loads until kGatStages - 1 are in flight: load `issued` goes to buffer
+    // issued % kGatStages, last read by the store of chunk issued - kGatStages <= done - 2
+    auto fill = [&]() {
+      while (issued - done < kGatStages - 1) {
+        if (p_idx == q_tail && !claim()) return;
+        const Body& b = q[p_idx % kGatQueue];
+        const long long left = b.bytes - p_off;
+        const uint32_t len = (uint32_t)(left < (long long)kGatChunk ? left : (long long)kGatChunk);
+        const int s = (int)(issued % kGatStages);
+        bulk_wait_read_all_but_one();
+        mbar_expect_tx(&full[s], len);
+        bulk_load(smem + (size_t)s * kGatChunk, b.src + p_off, len, &full[s]);
+        ++issued;
+        p_off += len;
+        if (p_off == b.bytes) {
+          ++p_idx;
+          p_off = 0;
+        }
+      }
+    };
+    fill();
+    while (done < issued) {
+      const Body& b = q[q_head % kGatQueue];
+      const long long left = b.bytes - c_off;
+      const uint32_t len = (uint32_t)(left < (long long)kGatChunk ? left : (long long)kGatChunk);
       const int s = (int)(done % kGatStages);
       if (!mbar_wait(&full[s], (uint32_t)((done / kGatStages) & 1))) {
         ok = false;
         break;
       }
-      bulk_store(dst, smem + (size_t)s * kGatChunk, len);
+      bulk_store(b.dst + c_off, smem + (size_t)s * kGatChunk, len);
       bulk_commit();
       ++done;
-      // the next load goes to the buffer of chunk done - 2, whose store is not the newest
-      bulk_wait_read_all_but_one();
-      issue();
+      c_off += len;
+      if (c_off == b.bytes) {
+        ++q_head;
+        c_off = 0;
+      }
+      fill();
     }
     // a wait that gave up: let every load still in flight land before the CTA exits
     for (long long k = done; k < issued; ++k)
       mbar_wait(&full[(int)(k % kGatStages)], (uint32_t)((k / kGatStages) & 1));
     bulk_wait_all();
     if (!ok && a.status) atomicExch(a.status, kStatusGatherWait);
+    // this CTA claims nothing more; the last one to get here resets the counter
+    __threadfence();
+    if (atomicAdd(&a.sched[1], 1ull) == (unsigned long long)gridDim.x - 1) {
+      a.sched[0] = 0;
+      a.sched[1] = 0;
+    }
   } else if (tid >= 32) {
     const int warp = tid / 32 - 1, lane = tid % 32, warps = kGatThreads / 32 - 1;
     int seg = 0;

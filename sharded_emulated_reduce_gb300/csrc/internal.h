@@ -11,6 +11,7 @@ namespace zero {
 constexpr int kThreads = 256;        // threads per CTA for every kernel
 constexpr int kMaxPartialBlocks = 1024;  // CTAs of the reduce kernel (one partial each)
 constexpr int kGatherSegs = 128;     // copy segments per gather launch
+constexpr int kGatherSlots = 64;     // tile-counter slots of the gather (a ring)
 
 // Scalars of one step, written by the finalize stage and read by the update kernel.
 struct DevScalars {
@@ -31,8 +32,9 @@ struct DevScaler {
   int32_t pad;
 };
 
-// One reduce CTA's statistics: the 128-bit sum of squares and the non-finite count.
-struct DevPartial {
+// One reduce CTA's statistics: the 128-bit sum of squares and the non-finite count
+// (16-byte aligned: the one-launch step reads each as two 16-byte vectors).
+struct alignas(16) DevPartial {
   unsigned long long lo, hi;
   long long bad;
   long long pad;
@@ -61,6 +63,9 @@ struct DevScratch {
   unsigned int ticket;    // arrival counter of the reduce CTAs
   int32_t gather_status;  // 0, or kStatusGatherWait after a gather wait expired
   unsigned int bar_count, bar_gen;  // grid barrier of the fused small-span step
+  // tile counters of the bulk-copy gather: {next tile to claim, CTAs finished} per slot;
+  // each launch takes the next slot of the ring, and its last CTA resets the slot to 0
+  unsigned long long gather_sched[kGatherSlots][2];
   DevPartial partials[kMaxPartialBlocks];
 };
 
@@ -103,6 +108,7 @@ struct GatherLaunch {
   int64_t tiles;       // total tiles over all segments
   int grid;
   int32_t* status;     // set to kStatusGatherWait if a bounded wait expires
+  unsigned long long* sched;  // this launch's {next tile, CTAs done} slot, zero at launch
   int realign;         // 1: every segment's source and destination differ in alignment
                        // modulo 16 bytes (k_gather_realign); 0: they agree (k_gather)
 };

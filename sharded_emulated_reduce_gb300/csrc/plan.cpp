@@ -76,6 +76,7 @@ struct zero_plan {
   // layer's copy runs there, so that it starts on the SMs the previous layer leaves
   cudaStream_t gside = nullptr;
   cudaEvent_t gev_fork = nullptr, gev_join = nullptr;
+  unsigned gather_launches = 0;  // picks each bulk-copy gather launch's tile-counter slot
   bool stepped = false;
 
   bool scaler_on = false;  // host mirror of the device scaler's on/off switch
@@ -358,6 +359,7 @@ struct GatherTables {
       t[k].tiles = 0;
       t[k].grid = 0;
       t[k].status = &p->scratch->gather_status;
+      t[k].sched = nullptr;
       t[k].realign = k;
     }
   }
@@ -365,6 +367,8 @@ struct GatherTables {
 
 int flush_gather(zero_plan* p, zero::GatherLaunch& gl, cudaStream_t s) {
   if (gl.nseg == 0) return ZERO_OK;
+  // the next slot of the ring of tile counters (each is zero again once its launch ends)
+  gl.sched = p->scratch->gather_sched[p->gather_launches++ % zero::kGatherSlots];
   EventPair ev;
   prof_begin(p, s, &ev);
   cudaError_t e = zero::launch_gather(gl, s);

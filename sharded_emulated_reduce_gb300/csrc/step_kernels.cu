@@ -154,6 +154,20 @@ __device__ __forceinline__ DevPre t_scalars(const DevScratch* st, long long t,
   return pre;
 }
 
+// x / L, rounded to nearest, for the fp32 loss scale L > 0. When L is a power of two
+// (as loss scales are in practice) this is the multiplication by the exact double 1 / L:
+// both round the same real number once, so the result is the same double, and a double
+// division is a long dependent sequence on this part.
+__device__ __forceinline__ double div_by_loss_scale(double x, float L) {
+  const unsigned b = __float_as_uint(L);
+  const unsigned e = (b >> 23) & 0xffu;
+  if ((b & 0x007fffffu) == 0u && e != 0u && e != 0xffu) {
+    const long long inv = (long long)(1023 + 127 - (int)e) << 52;  // 2^(127 - e)
+    return __dmul_rn(x, __longlong_as_double(inv));
+  }
+  return __ddiv_rn(x, (double)L);
+}
+
 // The step's scalars from its statistics (one thread), writing nothing: t and `scaler`
 // are the step counter and loss scaler before the step, *next the scaler after it.
 // Double arithmetic, each operation rounded to nearest, then one rounding to fp32.
@@ -177,7 +191,7 @@ __device__ __forceinline__ DevScalars make_scalars(long long t, DevScaler scaler
     sc.clip_coef = 1.0;
     sc.step = t;
   } else {
-    sc.norm = __ddiv_rn(__dsqrt_rn(sc.ss), (double)loss_scale);
+    sc.norm = div_by_loss_scale(__dsqrt_rn(sc.ss), loss_scale);
     double coef = 1.0;
     if (clip > 0.0f) {
       const double c = __ddiv_rn((double)clip, __dadd_rn(sc.norm, 1e-6));
@@ -186,7 +200,7 @@ __device__ __forceinline__ DevScalars make_scalars(long long t, DevScaler scaler
     sc.clip_coef = coef;
     sc.step = t + 1;
   }
-  sc.s = __double2float_rn(__ddiv_rn(sc.clip_coef, (double)loss_scale));
+  sc.s = __double2float_rn(div_by_loss_scale(sc.clip_coef, loss_scale));
   sc.omb1 = pre.omb1;
   sc.omb2 = pre.omb2;
   sc.bc1 = pre.bc1;
@@ -661,6 +675,7 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   __shared__ DevScalars s_sc;
   __shared__ long long s_t;
   __shared__ DevScaler s_scaler;
+  __shared__ DevPre s_pre;
   __shared__ int s_ok;
   DevScratch* st = a.r.st;
   const int tid = threadIdx.x;
@@ -689,6 +704,9 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   if (tid == 0) {
     s_t = st->step;  // before this CTA arrives at the barrier, so before any commit
     s_scaler = st->scaler;
+    // this step's t-only scalars, read while the CTA reduces (slot t & 1; this launch
+    // writes only slot (t + 1) & 1)
+    s_pre = load_pre(&st->pre[s_t & 1]);
     if (blockIdx.x == 0) st->sc.status = 0;
     if (state_bytes > 0) {  // the slice's state, on its way while the CTA reduces
       mbar_init(state_bar, 1);
@@ -741,10 +759,27 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   if (tid < 32) {
     U128 tot{0, 0};
     long long tb = 0;
-    for (int i = tid; i < (int)gridDim.x; i += 32) {
-      const DevPartial* p = &st->partials[i];
-      add128(tot, __ldcg(&p->lo), __ldcg(&p->hi));
-      tb += __ldcg(&p->bad);
+    // a lane's partials are all loaded before any is added: one round trip to L2 per
+    // pass of 32 * kPer partials (one pass for up to 256 SMs)
+    constexpr int kPer = 8;
+    for (int base = 0; base < (int)gridDim.x; base += 32 * kPer) {
+      longlong2 w[kPer][2];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = base + tid + 32 * k;
+        if (i < (int)gridDim.x) {
+          const longlong2* q = reinterpret_cast<const longlong2*>(&st->partials[i]);
+          w[k][0] = __ldcg(q);
+          w[k][1] = __ldcg(q + 1);
+        } else {
+          w[k][0] = w[k][1] = make_longlong2(0, 0);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        add128(tot, (unsigned long long)w[k][0].x, (unsigned long long)w[k][0].y);
+        tb += w[k][1].x;
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -756,7 +791,8 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     DevScaler next;
     DevScalars sc;
     if (tid == 0) {
-      const DevPre pre = t_scalars<false>(st, s_t, a.r.hp);
+      DevPre pre = s_pre;
+      if (!pre_matches(pre, s_t, a.r.hp)) pre = pre_scalars_call(s_t, a.r.hp);
       sc = make_scalars(s_t, s_scaler, tb, tot, a.r.loss_scale, a.r.clip, a.r.hp, pre, &next);
       s_sc = sc;
     }

@@ -84,6 +84,17 @@ def test_clip_off_and_on_and_mean_loss_scale():
         assert Runner(small(n=20_000, clip=clip, loss_scale=ls, cfg=170)).run().exact
 
 
+@pytest.mark.parametrize("ls", [1000.0, 3.0, 98304.0, 0.7, 2.0 ** -20, 2.0 ** 40])
+@pytest.mark.parametrize("n", [20_000, 5_000_003])
+def test_loss_scales_powers_of_two_and_others(ls, n):
+    # the norm and the unscale factor divide by the loss scale; a power of two is divided
+    # by multiplying with its exact reciprocal, any other scale by a division: both must
+    # give the oracle's bits (the fp16 gradients have sigma 1 whatever the scale); the
+    # 5M span runs the reduce and update kernels, the 20K span the one-launch step
+    w = small(n=n, loss_scale=ls, grad_sigma=1.0 / ls, clip=1.0, cfg=175)
+    assert Runner(w).run().exact
+
+
 def test_two_runs_are_bit_identical():
     outs = []
     for _ in range(2):
