@@ -47,10 +47,10 @@ struct AlTile {
 __device__ __forceinline__ AlTile al_tile(const GatherLaunch& a, int& seg, long long t) {
   while (seg + 1 < a.nseg && a.seg[seg + 1].tile_begin <= t) ++seg;
   const GatherSeg& sg = a.seg[seg];
-  const long long e0 = (t - sg.tile_begin) * kGatherTile;
+  const long long e0 = (t - sg.tile_begin) * kGatherTileAl;
   AlTile m;
   m.n = sg.len - e0;
-  if (m.n > kGatherTile) m.n = kGatherTile;
+  if (m.n > kGatherTileAl) m.n = kGatherTileAl;
   m.src = sg.src + e0;
   m.dst = sg.dst + e0;
   const uintptr_t sa = reinterpret_cast<uintptr_t>(m.src);

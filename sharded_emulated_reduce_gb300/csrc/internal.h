@@ -62,7 +62,7 @@ struct DevScratch {
   long long step;       // optimizer step counter t
   unsigned int ticket;    // arrival counter of the reduce CTAs
   int32_t gather_status;  // 0, or kStatusGatherWait after a gather wait expired
-  unsigned int bar_count, bar_gen;  // grid barrier of the fused small-span step
+  unsigned long long bar_arrivals;  // grid barrier of the fused small-span step (grows)
   // tile counters of the bulk-copy gather: {next tile to claim, CTAs finished} per slot;
   // each launch takes the next slot of the ring, and its last CTA resets the slot to 0
   unsigned long long gather_sched[kGatherSlots][2];
@@ -113,7 +113,8 @@ struct GatherLaunch {
                        // modulo 16 bytes (k_gather_realign); 0: they agree (k_gather)
 };
 
-constexpr int64_t kGatherTile = 32768;  // elements per gather tile (64 KiB)
+constexpr int64_t kGatherTile = 32768;    // elements per tile of the realigning gather (64 KiB)
+constexpr int64_t kGatherTileAl = 16384;  // elements per tile of the bulk-copy gather (32 KiB)
 constexpr int32_t kStatusGatherWait = 4;
 
 // *spare_cta (if given) is set to 1 when the launch carried the spare CTA that computes

@@ -107,8 +107,9 @@ extern "C" int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid,
   // The ticket of the last-arriving CTA and the grid barrier's words (which follow it)
   // must start at zero; the step counter is the caller's and is copied in and out
   // around the kernels.
-  static_assert(offsetof(DevScratch, bar_gen) - offsetof(DevScratch, ticket) ==
-                    3 * sizeof(unsigned), "ticket, gather status, barrier words are adjacent");
+  static_assert(offsetof(DevScratch, bar_arrivals) + sizeof(unsigned long long) -
+                    offsetof(DevScratch, ticket) == 4 * sizeof(unsigned),
+                "ticket, gather status and the barrier's arrival count are adjacent");
   e = cudaMemsetAsync(&st->ticket, 0, 4 * sizeof(unsigned), s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(&st->step, step_counter, sizeof(int64_t), cudaMemcpyDeviceToDevice, s);

@@ -401,7 +401,8 @@ int plan_layer(zero_plan* p, const int64_t* offs, int l, const void* const* shar
     sg.dst = dptr;
     sg.len = hi - lo;
     sg.tile_begin = gl.tiles;
-    gl.tiles += (sg.len + zero::kGatherTile - 1) / zero::kGatherTile;
+    const int64_t tile = k ? zero::kGatherTile : zero::kGatherTileAl;
+    gl.tiles += (sg.len + tile - 1) / tile;
   }
   return ZERO_OK;
 }
@@ -620,7 +621,7 @@ int zero_step_result(zero_plan* p, zero_step_info* out) {
   if (sc.status == zero::kStatusStepWait) {
     // the fused step's grid barrier gave up: its arrival count may be left part-way, so
     // start the next one from zero
-    cudaMemsetAsync(&p->scratch->bar_count, 0, 2 * sizeof(unsigned), p->last_stream);
+    cudaMemsetAsync(&p->scratch->bar_arrivals, 0, sizeof(unsigned long long), p->last_stream);
     cudaStreamSynchronize(p->last_stream);
   }
   if (sc.status != 0) return fail(ZERO_EDEVICE, "device status %d", sc.status);

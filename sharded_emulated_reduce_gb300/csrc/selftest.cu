@@ -26,16 +26,17 @@ __global__ void k_wait_probe(unsigned polls, int32_t* out) {
   if (threadIdx.x == 0) *out = arrived ? 0 : 1;
 }
 
-__global__ void k_barrier_probe(unsigned polls, int skip_one, unsigned* words, int32_t* out) {
+__global__ void k_barrier_probe(unsigned polls, int skip_one, unsigned long long* arrivals,
+                                int32_t* out) {
   if (threadIdx.x != 0) return;
   if (skip_one && blockIdx.x == 1) return;  // never arrives
-  const bool met = grid_barrier(&words[0], &words[1], gridDim.x, polls);
+  const bool met = grid_barrier(arrivals, gridDim.x, polls);
   if (blockIdx.x == 0) *out = met ? 0 : 1;
 }
 
 // Result word of the probe; host code gets its device address from cudaGetSymbolAddress.
 static __device__ int32_t g_probe_result;
-static __device__ unsigned g_probe_barrier[2];
+static __device__ unsigned long long g_probe_barrier;
 
 }  // namespace
 }  // namespace zero
@@ -68,7 +69,7 @@ extern "C" int zero_selftest_grid_barrier(uint32_t polls, int32_t skip_one, int3
   cudaError_t e = cudaGetSymbolAddress(&res, g_probe_result);
   if (e == cudaSuccess) e = cudaGetSymbolAddress(&words, g_probe_barrier);
   if (e == cudaSuccess) e = cudaMemset(res, 0xff, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMemset(words, 0, 2 * sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(words, 0, sizeof(unsigned long long));
   if (e != cudaSuccess) return set_error(ZERO_ECUDA, "self-test set-up failed");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
@@ -79,7 +80,7 @@ extern "C" int zero_selftest_grid_barrier(uint32_t polls, int32_t skip_one, int3
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, k_barrier_probe, (unsigned)polls, (int)(skip_one != 0),
-                         static_cast<unsigned*>(words), static_cast<int32_t*>(res));
+                         static_cast<unsigned long long*>(words), static_cast<int32_t*>(res));
   int32_t r = -1;
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(&r, res, sizeof r, cudaMemcpyDeviceToHost);

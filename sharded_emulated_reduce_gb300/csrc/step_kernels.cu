@@ -89,7 +89,8 @@ __device__ double u128_to_double(U128 a) {
   // bit 0 of top lies below the 53-bit significand's rounding bit, so or-ing the
   // dropped bits into it preserves round-to-nearest-even
   top |= (sticky != 0) ? 1ull : 0ull;
-  return ldexp(__ull2double_rn(top), shift);
+  // times 2^shift (1..64): an exact scaling by a power of two, as one multiply
+  return __dmul_rn(__ull2double_rn(top), __longlong_as_double((long long)(1023 + shift) << 52));
 }
 
 // The scalars that depend only on t and the hyperparameters: double arithmetic, each
@@ -600,8 +601,9 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
 //   3. unless the step is skipped, the CTA updates its slice from the sums it kept.
 // The fp32 sums never go to HBM and the step is one launch. A slice of at most
 // kSmallVecs groups also has its master/m/v brought into shared memory by bulk loads
-// issued at the start, so they arrive while the CTA reduces and waits at the barrier;
-// a longer slice reads them from global memory in the update. A 17th warp of CTA 0
+// issued once the CTA has arrived at the grid barrier, so they arrive while the CTAs wait
+// there and derive the scalars (DRAM is otherwise idle then); a longer slice reads them
+// from global memory in the update. A 17th warp of CTA 0
 // prepares the next step's t-only scalars meanwhile; it reads the step counter before
 // CTA 0 may advance it (named barrier 2), and the CTAs' own synchronisation uses named
 // barrier 1 over the 512 working threads only.
@@ -708,15 +710,23 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     // writes only slot (t + 1) & 1)
     s_pre = load_pre(&st->pre[s_t & 1]);
     if (blockIdx.x == 0) st->sc.status = 0;
-    if (state_bytes > 0) {  // the slice's state, on its way while the CTA reduces
+    if (state_bytes > 0) {
       mbar_init(state_bar, 1);
       mbar_fence_init();
+    }
+  }
+  // the slice's state is brought in by bulk loads issued once this CTA has arrived at the
+  // grid barrier (so that they compete neither with the reduce's loads nor with the
+  // barrier's own atomics); it arrives while the CTAs wait there and derive the scalars
+  auto issue_state_loads = [&]() {
+    if (tid == 0 && state_bytes > 0) {
       mbar_expect_tx(state_bar, 3 * state_bytes);
       bulk_load(s_master, a.master + e0, state_bytes, state_bar);
       bulk_load(s_m, a.m + e0, state_bytes, state_bar);
       bulk_load(s_v, a.v + e0, state_bytes, state_bar);
     }
-  }
+  };
+
   // every exit of thread 0 from here on first lets the state loads land (bounded)
   auto drain = [&]() { if (tid == 0 && state_bytes > 0) mbar_wait(state_bar, 0u); };
 
@@ -746,7 +756,7 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     st->partials[blockIdx.x].lo = acc.lo;
     st->partials[blockIdx.x].hi = acc.hi;
     st->partials[blockIdx.x].bad = bad;
-    s_ok = grid_barrier(&st->bar_count, &st->bar_gen, gridDim.x, kBarrierPolls) ? 1 : 0;
+    s_ok = grid_barrier(&st->bar_arrivals, gridDim.x, kBarrierPolls, issue_state_loads) ? 1 : 0;
   }
   bar_sync(1, kSmallThreads);
   if (!s_ok) {

@@ -1,7 +1,7 @@
 """CPU check of the gather's aligned-copy kernel: its tile claiming and ring, restated.
 
-The host cuts each layer at shard boundaries into segments and numbers 64 KiB tiles
-across them. In each CTA of the launch, thread 0 claims tiles from a shared counter (an
+The host cuts each layer at shard boundaries into segments and numbers fixed-size tiles
+across them (64 KiB; 32 KiB is checked too). In each CTA of the launch, thread 0 claims tiles from a shared counter (an
 atomic add), queues the ones with a 16-byte-aligned body, and streams the bodies, cut
 into chunks of at most 32 KiB, through a ring of S shared-memory buffers: it keeps S - 1
 loads in flight, stores chunk c from buffer c % S once it has landed, and issues the next
@@ -25,13 +25,13 @@ import random
 import numpy as np
 import pytest
 
-TILE = 32768            # elements per tile
+TILES = (32768, 16384)  # elements per tile (the kernel's, and a finer one)
 CHUNK = 32768           # bytes per ring buffer
 SHARD_BASE = 1 << 30    # synthetic byte addresses (16-byte aligned bases)
 LAYER_BASE = 1 << 50
 
 
-def plan_segments(offs, s, nd, shard_addr, layer_addr):
+def plan_segments(offs, s, nd, shard_addr, layer_addr, tile):
     """The host's cut: (src byte address, dst byte address, elements, first tile)."""
     segs, tiles = [], 0
     for l in range(len(offs) - 1):
@@ -44,16 +44,16 @@ def plan_segments(offs, s, nd, shard_addr, layer_addr):
                 dst = layer_addr[l] + 2 * (lo - a)
                 assert (src - dst) % 16 == 0  # the aligned class only
                 segs.append((src, dst, hi - lo, tiles))
-                tiles += -(-(hi - lo) // TILE)
+                tiles += -(-(hi - lo) // tile)
             r += 1
     return segs, tiles
 
 
-def tile_geom(segs, t):
+def tile_geom(segs, t, tile):
     seg = bisect.bisect_right([sg[3] for sg in segs], t) - 1
     src, dst, n_seg, first = segs[seg]
-    e0 = (t - first) * TILE
-    n = min(TILE, n_seg - e0)
+    e0 = (t - first) * tile
+    n = min(tile, n_seg - e0)
     sa, da = src + 2 * e0, dst + 2 * e0
     head = min(((16 - (da & 15)) & 15) >> 1, n)
     body = 0 if (sa + 2 * head) & 15 else ((n - head) >> 3) << 3
@@ -63,8 +63,8 @@ def tile_geom(segs, t):
 class Cta:
     """Thread 0 of one CTA: claim queue, producer (loads) and consumer (stores)."""
 
-    def __init__(self, stages, queue, segs, tiles, counter, copy):
-        self.S, self.Q = stages, queue
+    def __init__(self, stages, queue, segs, tiles, counter, copy, tile):
+        self.S, self.Q, self.tile = stages, queue, tile
         self.segs, self.tiles, self.counter, self.copy = segs, tiles, counter, copy
         self.q = [None] * queue
         self.q_head = self.q_tail = 0
@@ -84,7 +84,7 @@ class Cta:
                 break
             assert t > self.last_claim  # a CTA's claims increase (its segment index runs)
             self.last_claim = t
-            sa, da, n, head, body = tile_geom(self.segs, t)
+            sa, da, n, head, body = tile_geom(self.segs, t, self.tile)
             if body == 0:
                 continue
             self.q[self.q_tail % self.Q] = (sa + 2 * head, da + 2 * head, 2 * body)
@@ -141,15 +141,16 @@ def layout(rng):
     return nd, s, cuts
 
 
-@pytest.mark.parametrize("seed", range(3))
-@pytest.mark.parametrize("stages", [3, 6, 7])
-def test_claims_and_ring_cover_each_element_once(seed, stages):
-    rng = random.Random(seed * 10 + stages)
+@pytest.mark.parametrize("seed", range(2))
+@pytest.mark.parametrize("stages", [3, 4, 6, 7])
+@pytest.mark.parametrize("tile", TILES)
+def test_claims_and_ring_cover_each_element_once(seed, stages, tile):
+    rng = random.Random(seed * 10 + stages + tile)
     for _ in range(40):
         nd, s, offs = layout(rng)
         shard_addr = [SHARD_BASE + (r << 32) for r in range(nd)]
         layer_addr = [LAYER_BASE + (l << 32) for l in range(len(offs) - 1)]
-        segs, tiles = plan_segments(offs, s, nd, shard_addr, layer_addr)
+        segs, tiles = plan_segments(offs, s, nd, shard_addr, layer_addr, tile)
         if tiles == 0:
             continue
         grid = min(rng.choice([1, 2, 7, 152]), tiles)
@@ -167,7 +168,7 @@ def test_claims_and_ring_cover_each_element_once(seed, stages):
             written[l][j:j + m] += 1
 
         counter = [0]
-        ctas = [Cta(stages, stages + 2, segs, tiles, counter, copy) for _ in range(grid)]
+        ctas = [Cta(stages, stages + 2, segs, tiles, counter, copy, tile) for _ in range(grid)]
         for c in ctas:
             c.fill()
         live = list(ctas)
@@ -181,7 +182,7 @@ def test_claims_and_ring_cover_each_element_once(seed, stages):
         # the edge warps: heads and tails of every tile, split statically over the CTAs
         for b in range(grid):
             for t in range(b, tiles, grid):
-                sa, da, n, head, body = tile_geom(segs, t)
+                sa, da, n, head, body = tile_geom(segs, t, tile)
                 if body == 0:
                     copy(da, sa, n)
                     continue
