@@ -104,13 +104,14 @@ extern "C" int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid,
   float* gsum = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kCtrlBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // The ticket of the last-arriving CTA and the grid barrier's words (which follow it)
-  // must start at zero; the step counter is the caller's and is copied in and out
+  // The ticket of the last-arriving CTA, the grid barrier's arrival count and the
+  // reduce's tile counter (which follow it) must start at zero; the step counter is the caller's and is copied in and out
   // around the kernels.
-  static_assert(offsetof(DevScratch, bar_arrivals) + sizeof(unsigned long long) -
-                    offsetof(DevScratch, ticket) == 4 * sizeof(unsigned),
-                "ticket, gather status and the barrier's arrival count are adjacent");
-  e = cudaMemsetAsync(&st->ticket, 0, 4 * sizeof(unsigned), s);
+  static_assert(offsetof(DevScratch, reduce_next) + sizeof(unsigned long long) -
+                    offsetof(DevScratch, ticket) == 6 * sizeof(unsigned),
+                "ticket, gather status, the barrier's arrival count and the reduce's tile "
+                "counter are adjacent");
+  e = cudaMemsetAsync(&st->ticket, 0, 6 * sizeof(unsigned), s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(&st->step, step_counter, sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return bad(ZERO_ECUDA, "scratch set-up copy failed");

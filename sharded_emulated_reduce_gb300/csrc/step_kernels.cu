@@ -9,9 +9,12 @@
 //            non-finite count per CTA; the last CTA to finish combines them.
 //   update:  reads the sum and the fp32 master/m/v (16 B/param), writes master/m/v and
 //            the fp16 parameter (14 B/param).
-// The reduce is a persistent grid-stride loop over groups of 8 elements, one 16-byte
-// vector per rank per thread, coalesced across the warp. The update streams tiles through
-// shared memory with the TMA engine's 1-D bulk copies (see k_update).
+// For more than 8 ranks the reduce (k_reduce_bulk) stages the contribution streams through
+// a shared-memory ring with the TMA engine's 1-D bulk copies, a producer warp claiming
+// tiles and 8 consumer warps summing them; for 8 ranks or fewer (k_reduce) it is a
+// persistent grid-stride loop over groups of 8 elements, one 16-byte vector per rank per
+// thread, coalesced across the warp. The update streams tiles through shared memory with
+// bulk copies too (see k_update).
 //
 // The combine's scalars that depend only on the step counter (the bias corrections'
 // double-precision powers, slow on this part) are prepared one step ahead in a tagged
@@ -245,6 +248,13 @@ __device__ void compute_scalars(DevScratch* st, long long bad, U128 ss, float lo
   if (scaler.interval > 0) st->scaler = next;
 }
 
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Sum (acc, bad) over a CTA of NT threads; the result is valid in thread 0.
 template <int NT>
 __device__ void block_reduce(U128& acc, long long& bad) {
@@ -400,6 +410,288 @@ __global__ void __launch_bounds__(kThreads, (ND >= 32) ? 5 : 0)
   }
 }
 
+// ---- the bulk-load reduce --------------------------------------------------------------
+// The same rank-order sums, statistics and last-CTA combine as k_reduce, with the Nd
+// contribution streams staged through shared memory by TMA bulk copies instead of
+// register loads: a register-load reduce keeps at most its resident warps' loads in flight
+// (about 160 KB per SM at Nd = 64), while the bulk copies keep up to 160 KB in flight per
+// SM independent of registers and occupancy, the rate a pure bulk-copy read reaches.
+//
+// One CTA per SM: a producer warp and kRbConsumers consumer threads. A tile is kRbTile(RC)
+// groups of 8 elements; its ranks are taken RC at a time (RC = min(Nd, 8)), each chunk of
+// RC ranks one 32 KiB stage of a kRbStages-stage ring: RC bulk loads of the tile's slice of
+// RC consecutive ranks, rank-major in the stage. The producer claims tiles one at a time
+// from the plan's counter (so CTAs on slower SMs take fewer; the next claim is always in
+// flight while a tile's loads are issued), waits until a stage is empty,
+// records the tile in it and issues the loads; after the last tile it posts an end mark.
+// Each consumer thread owns groups tid + kRbConsumers * j of the tile and adds the chunks'
+// ranks in order, so the sums are the same rank-order fp32 additions as k_reduce's. Every
+// wait is bounded; a CTA whose wait expired publishes a non-finite count (the step is then
+// skipped) and a failure flag that the combine turns into kStatusReduceWait.
+constexpr int kRbConsumers = 256;
+constexpr int kRbThreads = kRbConsumers + 32;
+constexpr int kRbStages = 6;
+constexpr uint32_t kRbStageBytes = 32768;
+constexpr int32_t kStatusReduceWait = 3;
+// The bulk-load reduce serves more than 8 ranks. At 8 ranks or fewer the fp32 sums are a
+// fifth or more of its traffic, and storing them from one CTA's 8 consumer warps per SM
+// is slower than k_reduce, whose stores come from a full wave of warps.
+constexpr int kReduceBulkMinNd = 9;
+constexpr long long kRbFailBad = 1ll << 40;  // non-finite count a failed CTA publishes
+constexpr size_t kRbSmem = (size_t)kRbStages * kRbStageBytes + 2 * kRbStages * sizeof(uint64_t);
+
+template <int RC>
+struct RbGeom {
+  static constexpr int G = (RC >= 8) ? 1 : 8 / RC;        // groups per consumer per tile
+  static constexpr long long TG = (long long)kRbConsumers * G;  // groups per tile
+  static_assert(RC * TG * 16 <= kRbStageBytes, "a chunk fits its stage");
+};
+
+// Sum (acc, bad) over the kRbConsumers consumer threads (named barrier 1); thread 0 holds
+// the result.
+__device__ void rb_block_reduce(U128& acc, long long& bad) {
+  constexpr int W = kRbConsumers / 32;
+  __shared__ unsigned long long s_lo[W], s_hi[W];
+  __shared__ long long s_bad[W];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long lo = __shfl_xor_sync(0xffffffffu, acc.lo, o);
+    const unsigned long long hi = __shfl_xor_sync(0xffffffffu, acc.hi, o);
+    bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    add128(acc, lo, hi);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bar_sync(1, kRbConsumers);  // the shared arrays may still be read by a previous call
+  if (lane == 0) {
+    s_lo[warp] = acc.lo;
+    s_hi[warp] = acc.hi;
+    s_bad[warp] = bad;
+  }
+  bar_sync(1, kRbConsumers);
+  if (threadIdx.x == 0) {
+    U128 t{0, 0};
+    long long b = 0;
+    for (int w = 0; w < W; ++w) {
+      add128(t, s_lo[w], s_hi[w]);
+      b += s_bad[w];
+    }
+    acc = t;
+    bad = b;
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+// ND > 0: the rank count at compile time (RC = min(ND, 8) ranks per stage); ND == 0: the
+// count from the arguments, 8 ranks per stage (the last chunk may hold fewer).
+template <int ND, int CAP, bool PRE>
+__global__ void __launch_bounds__(kRbThreads, 1)
+    k_reduce_bulk(const __grid_constant__ ReduceArgs<CAP> a, unsigned long long* next_tile) {
+  constexpr int RC = (ND > 0 && ND < 8) ? ND : 8;
+  using Geo = RbGeom<RC>;
+  constexpr int G = Geo::G;
+  constexpr long long TG = Geo::TG;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kRbStages * kRbStageBytes);
+  uint64_t* empty = full + kRbStages;
+  __shared__ long long s_tile[kRbStages];  // the stage's tile, or -1: no more tiles
+  __shared__ int s_chunk[kRbStages];       // which chunk of the tile's ranks
+  __shared__ int s_fail;
+  DevScratch* st = a.st;
+  const int tid = threadIdx.x;
+  if constexpr (PRE) {
+    if (blockIdx.x == 0) {  // no reduce work: the next step's t-only scalars
+      if (tid == 0) {
+        const long long tn = st->step + 1;
+        DevPre* slot = &st->pre[tn & 1];
+        if (!pre_matches(load_pre(slot), tn, a.hp)) *slot = pre_scalars_call(tn, a.hp);
+      }
+      return;
+    }
+  }
+  const int nd = ND > 0 ? ND : a.nd;
+  const int nchunks = (nd + RC - 1) / RC;
+  const long long tiles = (a.n_vec + TG - 1) / TG;
+  const unsigned nred = gridDim.x - (PRE ? 1u : 0u);
+  const unsigned b = blockIdx.x - (PRE ? 1u : 0u);
+  if (tid == 0) {
+    for (int s = 0; s < kRbStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kRbConsumers / 32);
+    }
+    mbar_fence_init();
+    s_fail = 0;
+  }
+  __syncthreads();
+
+  if (tid >= kRbConsumers) {  // the producer warp
+    if (tid == kRbConsumers) {
+      long long q = 0;  // stages issued
+      bool ok = true;
+      auto take_stage = [&](int* s_out) {  // the next stage, once its consumers are done
+        const int s = (int)(q % kRbStages);
+        if (q >= kRbStages &&
+            !mbar_wait(&empty[s], (uint32_t)(((q / kRbStages) - 1) & 1))) {
+          ok = false;
+          return false;
+        }
+        *s_out = s;
+        return true;
+      };
+      // the claim of the next tile is issued before this tile's loads, so that its round
+      // trip overlaps them (a tile is a single stage when Nd <= 8)
+      long long t = (long long)atomicAdd(next_tile, 1ull);
+      for (; t < tiles; ) {
+        const long long t_after = (long long)atomicAdd(next_tile, 1ull);
+        const long long v0 = t * TG;
+        const long long nv = a.n_vec - v0 < TG ? a.n_vec - v0 : TG;
+        const uint32_t bytes = (uint32_t)(nv * 16);
+        for (int k = 0; k < nchunks && ok; ++k) {
+          int s;
+          if (!take_stage(&s)) break;
+          const int r0 = k * RC;
+          const int nr = nd - r0 < RC ? nd - r0 : RC;
+          s_tile[s] = t;
+          s_chunk[s] = k;
+          mbar_expect_tx(&full[s], bytes * (uint32_t)nr);
+          unsigned char* dst = smem + (size_t)s * kRbStageBytes;
+          for (int j = 0; j < nr; ++j)
+            bulk_load(dst + (size_t)j * TG * 16,
+                      reinterpret_cast<const unsigned char*>(a.g[r0 + j]) + v0 * 16, bytes,
+                      &full[s]);
+          ++q;
+        }
+        if (!ok) break;
+        t = t_after;
+      }
+      int s;
+      if (ok && take_stage(&s)) {  // the end mark
+        s_tile[s] = -1;
+        mbar_arrive(&full[s]);
+        ++q;
+      }
+      if (!ok) {
+        atomicExch(&s_fail, 1);
+        // let the loads of the last kRbStages issued stages land before the CTA ends
+        for (long long k = q > kRbStages ? q - kRbStages : 0; k < q; ++k)
+          mbar_wait(&full[(int)(k % kRbStages)], (uint32_t)((k / kRbStages) & 1));
+      }
+    }
+    return;
+  }
+
+  // the consumers
+  U128 acc{0, 0};
+  long long bad = 0;
+  float s[G][8];
+  long long q = 0;  // stages consumed
+  const int warp = tid >> 5, lane = tid & 31;
+  for (;;) {
+    const int si = (int)(q % kRbStages);
+    if (!mbar_wait(&full[si], (uint32_t)((q / kRbStages) & 1))) {
+      atomicExch(&s_fail, 1);
+      break;
+    }
+    const long long t = s_tile[si];
+    if (t < 0) break;
+    const int k = s_chunk[si];
+    if (k == 0) {
+#pragma unroll
+      for (int j = 0; j < G; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[j][e] = 0.0f;
+    }
+    const int r0 = k * RC;
+    const int nr = nd - r0 < RC ? nd - r0 : RC;
+    const long long v0 = t * TG;
+    const long long nv = a.n_vec - v0 < TG ? a.n_vec - v0 : TG;
+    const uint4* w = reinterpret_cast<const uint4*>(smem + (size_t)si * kRbStageBytes);
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const long long g = tid + (long long)kRbConsumers * j;
+      if (g < nv) {
+        if (ND > 0 && RC == nr) {
+#pragma unroll
+          for (int r = 0; r < RC; ++r) add_vec(s[j], w[r * TG + g]);
+        } else {
+          for (int r = 0; r < nr; ++r) add_vec(s[j], w[r * TG + g]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[si]);
+    ++q;
+    if (k == nchunks - 1) {  // the tile's sums are complete
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const long long g = tid + (long long)kRbConsumers * j;
+        if (g >= nv) continue;
+        const long long v = v0 + g;
+        const long long base = v * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (base + e >= a.n_valid) s[j][e] = 0.0f;  // padding: not a parameter
+          const bool fin = is_finite(s[j][e]);
+          bad += fin ? 0 : 1;
+          add_square(acc, fin ? s[j][e] : 0.0f);
+        }
+        float4* o = reinterpret_cast<float4*>(a.gsum) + 2 * v;
+        o[0] = make_float4(s[j][0], s[j][1], s[j][2], s[j][3]);
+        o[1] = make_float4(s[j][4], s[j][5], s[j][6], s[j][7]);
+      }
+    }
+  }
+  (void)warp;
+
+  // CTA partial, then the last CTA to arrive combines all partials (no waiting)
+  rb_block_reduce(acc, bad);
+  __shared__ int s_last;
+  if (tid == 0) {
+    const int failed = s_fail;
+    st->partials[b].lo = acc.lo;
+    st->partials[b].hi = acc.hi;
+    st->partials[b].bad = bad + (failed ? kRbFailBad : 0);
+    st->partials[b].pad = failed;
+    __threadfence();
+    const unsigned prev = atomicAdd(&st->ticket, 1u);
+    s_last = prev == nred - 1;
+  }
+  bar_sync(1, kRbConsumers);
+  if (!s_last) return;
+  __threadfence();
+  U128 tot{0, 0};
+  long long tb = 0;
+  long long tf = 0;
+  for (int i = tid; i < (int)nred; i += kRbConsumers) {
+    const DevPartial* p = &st->partials[i];
+    add128(tot, __ldcg(&p->lo), __ldcg(&p->hi));
+    tb += __ldcg(&p->bad);
+    tf += __ldcg(&p->pad);
+  }
+  bad = tb;
+  rb_block_reduce(tot, bad);
+  // the failure flags, summed the same way (their 128-bit part unused)
+  U128 dummy{0, 0};
+  rb_block_reduce(dummy, tf);
+  if (tid == 0) {
+    st->stats[0] = bad;
+    st->stats[1] = (long long)(tot.lo & 0xffffffffull);
+    st->stats[2] = (long long)(tot.lo >> 32);
+    st->stats[3] = (long long)(tot.hi & 0xffffffffull);
+    st->stats[4] = (long long)(tot.hi >> 32);
+    st->stats[5] = tf;  // CTAs whose bounded wait expired (0 on a healthy GPU)
+    st->stats[6] = st->stats[7] = 0;
+    if (a.finalize) {
+      compute_scalars<!PRE>(st, bad, tot, a.loss_scale, a.clip, a.hp);
+      if (tf != 0) st->sc.status = kStatusReduceWait;
+    }
+    *next_tile = 0;  // every producer has made its last claim
+    st->ticket = 0;
+  }
+}
+
 // Scalars from the exchange buffer, after the caller's all-reduce (one thread).
 __global__ void k_finalize(DevScratch* st, float loss_scale, float clip, HostHParams hp) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
@@ -415,6 +707,7 @@ __global__ void k_finalize(DevScratch* st, float loss_scale, float clip, HostHPa
     }
   }
   compute_scalars<false>(st, bad, ss, loss_scale, clip, hp);
+  if (st->stats[5] != 0) st->sc.status = kStatusReduceWait;  // a reduce CTA's wait expired
 }
 
 // The t-only scalars for the counter now in the scratch (the next step's), off the
@@ -625,13 +918,6 @@ struct SmallArgs {
   uint16_t* p16;
   long long vecs_per_cta;
 };
-
-__device__ __forceinline__ void bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bar_arrive(int id, int n) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // Sum (acc, bad) over the CTA's kSmallThreads working threads (named barrier 1); the
 // result is valid in thread 0.
@@ -987,20 +1273,69 @@ cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
   return cudaGetLastError();
 }
 
+template <int ND, int CAP>
+cudaError_t go_reduce_bulk(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
+  ReduceArgs<CAP> a;
+  for (int r = 0; r < CAP; ++r) a.g[r] = r < p.nd ? p.grads[r] : nullptr;
+  a.gsum = p.gsum;
+  a.n_vec = p.n_span / 8;
+  a.n_valid = p.n_valid;
+  a.st = p.scratch;
+  a.loss_scale = p.loss_scale;
+  a.clip = p.clip;
+  a.hp = p.hp;
+  a.nd = p.nd;
+  a.finalize = p.finalize ? 1 : 0;
+  static std::atomic<bool> attr_set[kMaxDevices];
+  int dev = 0;
+  const int sms = sm_count(&dev);
+  if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_relaxed)) {
+    cudaError_t e = cudaFuncSetAttribute(k_reduce_bulk<ND, CAP, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRbSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_reduce_bulk<ND, CAP, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRbSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_relaxed);
+  }
+  constexpr int RC = (ND > 0 && ND < 8) ? ND : 8;
+  const long long tiles = (a.n_vec + RbGeom<RC>::TG - 1) / RbGeom<RC>::TG;
+  // one CTA per SM, at most one per tile; a grid below one wave gets one more CTA that
+  // computes the next step's t-only scalars while the others reduce
+  long long grid = sms;
+  if (p.grid > 0 && p.grid < grid) grid = p.grid;
+  if (grid > tiles) grid = tiles;
+  if (grid > kMaxPartialBlocks) grid = kMaxPartialBlocks;
+  if (grid < 1) grid = 1;
+  const bool pre = grid < sms;
+  if (spare_cta) *spare_cta = pre ? 1 : 0;
+  unsigned long long* next_tile = &p.scratch->reduce_next;
+  if (pre)
+    k_reduce_bulk<ND, CAP, true><<<(unsigned)grid + 1, kRbThreads, kRbSmem, s>>>(a, next_tile);
+  else
+    k_reduce_bulk<ND, CAP, false><<<(unsigned)grid, kRbThreads, kRbSmem, s>>>(a, next_tile);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
-  switch (p.nd) {
+  if (p.nd >= kReduceBulkMinNd) {
+    switch (p.nd) {
+      case 16: return go_reduce_bulk<16, 16>(p, s, spare_cta);
+      case 32: return go_reduce_bulk<32, 64>(p, s, spare_cta);
+      case 64: return go_reduce_bulk<64, 64>(p, s, spare_cta);
+      default:
+        if (p.nd <= 64) return go_reduce_bulk<0, 64>(p, s, spare_cta);
+        return go_reduce_bulk<0, ZERO_MAX_ND>(p, s, spare_cta);
+    }
+  }
+  switch (p.nd) {  // 8 ranks or fewer: the register-load reduce
     case 1: return go_reduce<1, 16>(p, s, spare_cta);
     case 2: return go_reduce<2, 16>(p, s, spare_cta);
     case 4: return go_reduce<4, 16>(p, s, spare_cta);
     case 8: return go_reduce<8, 16>(p, s, spare_cta);
-    case 16: return go_reduce<16, 16>(p, s, spare_cta);
-    case 32: return go_reduce<32, 64>(p, s, spare_cta);
-    case 64: return go_reduce<64, 64>(p, s, spare_cta);
-    default:
-      if (p.nd <= 64) return go_reduce<0, 64>(p, s, spare_cta);
-      return go_reduce<0, ZERO_MAX_ND>(p, s, spare_cta);
+    default: return go_reduce<0, 16>(p, s, spare_cta);
   }
 }
 
