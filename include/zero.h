@@ -70,9 +70,11 @@ typedef struct {
   int32_t overflow;   /* 1 if any summed gradient in the span was inf or nan          */
   int32_t skipped;    /* 1 if the update was not applied (overflow or status != 0)    */
   int32_t status;     /* 0, or a device-side failure code: 2 = a bulk load of the
-                       * update did not arrive within its bounded wait; 5 = the grid
-                       * barrier of the one-launch small-span step gave up (the update
-                       * may be partly applied; neither is expected on a healthy GPU)   */
+                       * update did not arrive within its bounded wait; 3 = a bulk load
+                       * or stage wait of the reduce (8 ranks or more) did not complete
+                       * in time (the step is then skipped, the state untouched); 5 = the
+                       * grid barrier of the one-launch small-span step gave up (the
+                       * update may be partly applied). None is expected on a healthy GPU. */
   int32_t reserved;
   int64_t step;       /* optimizer step counter after the step                        */
   double global_norm; /* L2 norm of the unscaled summed gradient (+inf on overflow)   */
@@ -194,7 +196,8 @@ int zero_shard_reduce(zero_plan* plan, int32_t r0, int32_t r1, const void* const
 /* The plan's exchange buffer: ZERO_STATS_WORDS int64 on the device, written by
  * zero_shard_reduce: word 0 counts non-finite summed gradients, words 1..4 hold the
  * exact sum of squares of (gsum * 2^24) as four 32-bit limbs (least significant first),
- * words 5..7 are zero. Summing the buffers of all processes word by word (an integer
+ * word 5 counts reduce CTAs whose bounded wait expired (0 on a healthy GPU; such a CTA also
+ * adds a large count to word 0, so the step is skipped), words 6..7 are zero. Summing the buffers of all processes word by word (an integer
  * all-reduce) gives the statistics of the whole buffer. Valid after zero_plan_bind. */
 int zero_shard_stats(zero_plan* plan, void** dev_words);
 

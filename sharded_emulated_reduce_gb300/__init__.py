@@ -303,7 +303,8 @@ def rank_ranges(nd: int, world: int) -> list[tuple[int, int]]:
 def stats_words(nonfinite: int, sum_sq: int) -> list[int]:
     """Host view of the exchange-buffer format (zero_shard_stats): word 0 the non-finite
     count, words 1..4 the 32-bit limbs of the exact sum of squares of (gsum * 2^24),
-    least significant first, words 5..7 zero."""
+    least significant first, word 5 the count of reduce CTAs whose bounded wait expired
+    (0 here), words 6..7 zero."""
     return [nonfinite] + [(sum_sq >> (32 * i)) & 0xFFFFFFFF for i in range(4)] + [0, 0, 0]
 
 

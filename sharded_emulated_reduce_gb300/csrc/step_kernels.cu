@@ -412,45 +412,54 @@ __global__ void __launch_bounds__(kThreads, (ND >= 32) ? 5 : 0)
 
 // ---- the bulk-load reduce --------------------------------------------------------------
 // The same rank-order sums, statistics and last-CTA combine as k_reduce, with the Nd
-// contribution streams staged through shared memory by TMA bulk copies instead of
-// register loads: a register-load reduce keeps at most its resident warps' loads in flight
-// (about 160 KB per SM at Nd = 64), while the bulk copies keep up to 160 KB in flight per
-// SM independent of registers and occupancy, the rate a pure bulk-copy read reaches.
+// contribution streams staged through shared memory by TMA bulk copies instead of register
+// loads. A register-load reduce keeps only its resident warps' loads in flight (about
+// 160 KB per SM at Nd = 64, at 61% occupancy); the bulk copies keep five 32 KiB stages in
+// flight per SM whatever the registers and occupancy, which is what a pure bulk-copy read
+// needs to reach its rate on this part.
 //
-// One CTA per SM: a producer warp and kRbConsumers consumer threads. A tile is kRbTile(RC)
-// groups of 8 elements; its ranks are taken RC at a time (RC = min(Nd, 8)), each chunk of
-// RC ranks one 32 KiB stage of a kRbStages-stage ring: RC bulk loads of the tile's slice of
-// RC consecutive ranks, rank-major in the stage. The producer claims tiles one at a time
-// from the plan's counter (so CTAs on slower SMs take fewer; the next claim is always in
-// flight while a tile's loads are issued), waits until a stage is empty,
-// records the tile in it and issues the loads; after the last tile it posts an end mark.
-// Each consumer thread owns groups tid + kRbConsumers * j of the tile and adds the chunks'
-// ranks in order, so the sums are the same rank-order fp32 additions as k_reduce's. Every
-// wait is bounded; a CTA whose wait expired publishes a non-finite count (the step is then
-// skipped) and a failure flag that the combine turns into kStatusReduceWait.
-constexpr int kRbConsumers = 256;
-constexpr int kRbThreads = kRbConsumers + 32;
+// One CTA per SM: a producer warp and CONS consumer threads. A tile is TG groups of 8
+// elements (TG = CONS when Nd is at least kRanks = 2048 / CONS). Its ranks are taken RC at a
+// time (RC = min(Nd, kRanks)), each chunk of RC ranks one 32 KiB stage of a kRbStages-stage
+// ring: RC bulk loads of the tile's slice of RC consecutive ranks, rank-major in the stage.
+// The producer claims tiles one at a time from the plan's counter (so CTAs on slower SMs
+// take fewer; the next claim is always in flight while a tile's loads are issued), waits
+// until a stage is empty, records the tile in it and issues the loads; after the last tile
+// it posts an end mark. Each consumer thread owns groups tid + CONS * j of the tile and
+// adds the chunks' ranks in order, so the sums are the same rank-order fp32 additions as
+// k_reduce's. The consumers' work per byte (the exact sum of squares per element) is
+// latency-bound at few warps, so 8 ranks, whose sums are a fifth of the traffic, use 512
+// consumers; more ranks use 256. Every wait is bounded; a CTA whose wait expired publishes a
+// non-finite count (the step is then skipped) and a failure flag that the combine turns
+// into kStatusReduceWait.
 constexpr int kRbStages = 6;
 constexpr uint32_t kRbStageBytes = 32768;
 constexpr int32_t kStatusReduceWait = 3;
-// The bulk-load reduce serves more than 8 ranks. At 8 ranks or fewer the fp32 sums are a
-// fifth or more of its traffic, and storing them from one CTA's 8 consumer warps per SM
-// is slower than k_reduce, whose stores come from a full wave of warps.
-constexpr int kReduceBulkMinNd = 9;
+
 constexpr long long kRbFailBad = 1ll << 40;  // non-finite count a failed CTA publishes
 constexpr size_t kRbSmem = (size_t)kRbStages * kRbStageBytes + 2 * kRbStages * sizeof(uint64_t);
 
-template <int RC>
+// CONS consumer threads take one group each from every rank of a stage: a 32 KiB stage
+// then holds kRanks = 2048 / CONS ranks of a tile of CONS groups.
+template <int CONS>
+struct RbCfg {
+  static constexpr int kRanks = 2048 / CONS;
+  static constexpr int kThreads = CONS + 32;  // + the producer warp
+};
+
+template <int RC, int CONS>
 struct RbGeom {
-  static constexpr int G = (RC >= 8) ? 1 : 8 / RC;        // groups per consumer per tile
-  static constexpr long long TG = (long long)kRbConsumers * G;  // groups per tile
+  static constexpr int R = RbCfg<CONS>::kRanks;
+  static constexpr int G = (RC >= R) ? 1 : R / RC;           // groups per consumer per tile
+  static constexpr long long TG = (long long)CONS * G;       // groups per tile
   static_assert(RC * TG * 16 <= kRbStageBytes, "a chunk fits its stage");
 };
 
-// Sum (acc, bad) over the kRbConsumers consumer threads (named barrier 1); thread 0 holds
-// the result.
+// Sum (acc, bad) over the CONS consumer threads (named barrier 1); thread 0 holds the
+// result.
+template <int CONS>
 __device__ void rb_block_reduce(U128& acc, long long& bad) {
-  constexpr int W = kRbConsumers / 32;
+  constexpr int W = CONS / 32;
   __shared__ unsigned long long s_lo[W], s_hi[W];
   __shared__ long long s_bad[W];
 #pragma unroll
@@ -461,13 +470,13 @@ __device__ void rb_block_reduce(U128& acc, long long& bad) {
     add128(acc, lo, hi);
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  bar_sync(1, kRbConsumers);  // the shared arrays may still be read by a previous call
+  bar_sync(1, CONS);  // the shared arrays may still be read by a previous call
   if (lane == 0) {
     s_lo[warp] = acc.lo;
     s_hi[warp] = acc.hi;
     s_bad[warp] = bad;
   }
-  bar_sync(1, kRbConsumers);
+  bar_sync(1, CONS);
   if (threadIdx.x == 0) {
     U128 t{0, 0};
     long long b = 0;
@@ -484,13 +493,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
 }
 
-// ND > 0: the rank count at compile time (RC = min(ND, 8) ranks per stage); ND == 0: the
-// count from the arguments, 8 ranks per stage (the last chunk may hold fewer).
-template <int ND, int CAP, bool PRE>
-__global__ void __launch_bounds__(kRbThreads, 1)
+// ND > 0: the rank count at compile time (RC = min(ND, kRanks) ranks per stage); ND == 0:
+// the count from the arguments, kRanks ranks per stage (the last chunk may hold fewer).
+template <int ND, int CAP, bool PRE, int CONS>
+__global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
     k_reduce_bulk(const __grid_constant__ ReduceArgs<CAP> a, unsigned long long* next_tile) {
-  constexpr int RC = (ND > 0 && ND < 8) ? ND : 8;
-  using Geo = RbGeom<RC>;
+  constexpr int kRbConsumers = CONS;
+  constexpr int RC = (ND > 0 && ND < RbCfg<CONS>::kRanks) ? ND : RbCfg<CONS>::kRanks;
+  using Geo = RbGeom<RC, CONS>;
   constexpr int G = Geo::G;
   constexpr long long TG = Geo::TG;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -646,7 +656,7 @@ __global__ void __launch_bounds__(kRbThreads, 1)
   (void)warp;
 
   // CTA partial, then the last CTA to arrive combines all partials (no waiting)
-  rb_block_reduce(acc, bad);
+  rb_block_reduce<CONS>(acc, bad);
   __shared__ int s_last;
   if (tid == 0) {
     const int failed = s_fail;
@@ -671,10 +681,10 @@ __global__ void __launch_bounds__(kRbThreads, 1)
     tf += __ldcg(&p->pad);
   }
   bad = tb;
-  rb_block_reduce(tot, bad);
+  rb_block_reduce<CONS>(tot, bad);
   // the failure flags, summed the same way (their 128-bit part unused)
   U128 dummy{0, 0};
-  rb_block_reduce(dummy, tf);
+  rb_block_reduce<CONS>(dummy, tf);
   if (tid == 0) {
     st->stats[0] = bad;
     st->stats[1] = (long long)(tot.lo & 0xffffffffull);
@@ -1273,7 +1283,7 @@ cudaError_t go_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
   return cudaGetLastError();
 }
 
-template <int ND, int CAP>
+template <int ND, int CAP, int CONS>
 cudaError_t go_reduce_bulk(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
   ReduceArgs<CAP> a;
   for (int r = 0; r < CAP; ++r) a.g[r] = r < p.nd ? p.grads[r] : nullptr;
@@ -1290,16 +1300,16 @@ cudaError_t go_reduce_bulk(const ReduceLaunch& p, cudaStream_t s, int* spare_cta
   int dev = 0;
   const int sms = sm_count(&dev);
   if (dev < 0 || dev >= kMaxDevices || !attr_set[dev].load(std::memory_order_relaxed)) {
-    cudaError_t e = cudaFuncSetAttribute(k_reduce_bulk<ND, CAP, false>,
+    cudaError_t e = cudaFuncSetAttribute(k_reduce_bulk<ND, CAP, false, CONS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRbSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_reduce_bulk<ND, CAP, true>,
+      e = cudaFuncSetAttribute(k_reduce_bulk<ND, CAP, true, CONS>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRbSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true, std::memory_order_relaxed);
   }
-  constexpr int RC = (ND > 0 && ND < 8) ? ND : 8;
-  const long long tiles = (a.n_vec + RbGeom<RC>::TG - 1) / RbGeom<RC>::TG;
+  constexpr int RC = (ND > 0 && ND < RbCfg<CONS>::kRanks) ? ND : RbCfg<CONS>::kRanks;
+  const long long tiles = (a.n_vec + RbGeom<RC, CONS>::TG - 1) / RbGeom<RC, CONS>::TG;
   // one CTA per SM, at most one per tile; a grid below one wave gets one more CTA that
   // computes the next step's t-only scalars while the others reduce
   long long grid = sms;
@@ -1310,32 +1320,31 @@ cudaError_t go_reduce_bulk(const ReduceLaunch& p, cudaStream_t s, int* spare_cta
   const bool pre = grid < sms;
   if (spare_cta) *spare_cta = pre ? 1 : 0;
   unsigned long long* next_tile = &p.scratch->reduce_next;
+  constexpr int kThreads = RbCfg<CONS>::kThreads;
   if (pre)
-    k_reduce_bulk<ND, CAP, true><<<(unsigned)grid + 1, kRbThreads, kRbSmem, s>>>(a, next_tile);
+    k_reduce_bulk<ND, CAP, true, CONS><<<(unsigned)grid + 1, kThreads, kRbSmem, s>>>(a, next_tile);
   else
-    k_reduce_bulk<ND, CAP, false><<<(unsigned)grid, kRbThreads, kRbSmem, s>>>(a, next_tile);
+    k_reduce_bulk<ND, CAP, false, CONS><<<(unsigned)grid, kThreads, kRbSmem, s>>>(a, next_tile);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_reduce(const ReduceLaunch& p, cudaStream_t s, int* spare_cta) {
-  if (p.nd >= kReduceBulkMinNd) {
-    switch (p.nd) {
-      case 16: return go_reduce_bulk<16, 16>(p, s, spare_cta);
-      case 32: return go_reduce_bulk<32, 64>(p, s, spare_cta);
-      case 64: return go_reduce_bulk<64, 64>(p, s, spare_cta);
-      default:
-        if (p.nd <= 64) return go_reduce_bulk<0, 64>(p, s, spare_cta);
-        return go_reduce_bulk<0, ZERO_MAX_ND>(p, s, spare_cta);
-    }
-  }
-  switch (p.nd) {  // 8 ranks or fewer: the register-load reduce
+  // 8 ranks: the bulk-load reduce with 512 consumers (4 ranks per stage); more: with 256
+  // (8 ranks per stage); fewer: the register-load reduce
+  switch (p.nd) {
     case 1: return go_reduce<1, 16>(p, s, spare_cta);
     case 2: return go_reduce<2, 16>(p, s, spare_cta);
     case 4: return go_reduce<4, 16>(p, s, spare_cta);
-    case 8: return go_reduce<8, 16>(p, s, spare_cta);
-    default: return go_reduce<0, 16>(p, s, spare_cta);
+    case 8: return go_reduce_bulk<8, 16, 512>(p, s, spare_cta);
+    case 16: return go_reduce_bulk<16, 16, 256>(p, s, spare_cta);
+    case 32: return go_reduce_bulk<32, 64, 256>(p, s, spare_cta);
+    case 64: return go_reduce_bulk<64, 64, 256>(p, s, spare_cta);
+    default:
+      if (p.nd < 8) return go_reduce<0, 16>(p, s, spare_cta);
+      if (p.nd <= 64) return go_reduce_bulk<0, 64, 256>(p, s, spare_cta);
+      return go_reduce_bulk<0, ZERO_MAX_ND, 256>(p, s, spare_cta);
   }
 }
 

@@ -20,20 +20,20 @@ import random
 
 import pytest
 
-CONSUMERS = 256
 STAGE_BYTES = 32768
 
 
-def geometry(nd, nd_static):
-    rc = nd_static if 0 < nd_static < 8 else 8
-    g = 1 if rc >= 8 else 8 // rc
-    return rc, g, CONSUMERS * g
+def geometry(nd, nd_static, consumers):
+    ranks = 2048 // consumers  # ranks per 32 KiB stage, one group per consumer
+    rc = nd_static if 0 < nd_static < ranks else ranks
+    g = 1 if rc >= ranks else ranks // rc
+    return rc, g, consumers * g
 
 
 class Cta:
-    def __init__(self, nd, nd_static, n_vec, stages, counter, log):
-        self.nd, self.n_vec, self.S = nd, n_vec, stages
-        self.rc, self.g, self.tg = geometry(nd, nd_static)
+    def __init__(self, nd, nd_static, n_vec, stages, counter, log, consumers):
+        self.nd, self.n_vec, self.S, self.consumers = nd, n_vec, stages, consumers
+        self.rc, self.g, self.tg = geometry(nd, nd_static, consumers)
         self.tiles = -(-n_vec // self.tg)
         self.nchunks = -(-nd // self.rc)
         self.counter, self.log = counter, log
@@ -99,9 +99,9 @@ class Cta:
         v0 = t * self.tg
         nv = min(self.tg, self.n_vec - v0)
         nr = min(self.rc, self.nd - k * self.rc)
-        for c in range(CONSUMERS):
+        for c in range(self.consumers):
             for j in range(self.g):
-                gi = c + CONSUMERS * j
+                gi = c + self.consumers * j
                 if gi >= nv:
                     continue
                 v = v0 + gi
@@ -114,19 +114,20 @@ class Cta:
         return True
 
 
-# the rank counts the library sends to this kernel (more than 8): 16, 32 and 64 with the
-# count fixed at compile time, the others read at run time
-@pytest.mark.parametrize("nd,nd_static", [(16, 16), (32, 32), (64, 64), (9, 0), (17, 0),
+# the rank counts the library sends to this kernel: 8, 16, 32 and 64 with the count fixed
+# at compile time, the others read at run time
+@pytest.mark.parametrize("nd,nd_static", [(8, 8), (16, 16), (32, 32), (64, 64), (9, 0), (17, 0),
                                           (100, 0), (256, 0)])
 @pytest.mark.parametrize("stages", [3, 6])
-def test_every_group_sums_all_ranks_once_in_order(nd, nd_static, stages):
-    rng = random.Random(nd * 7 + stages)
+@pytest.mark.parametrize("consumers", [256, 512])
+def test_every_group_sums_all_ranks_once_in_order(nd, nd_static, stages, consumers):
+    rng = random.Random(nd * 7 + stages + consumers)
     for n_vec in [1, 255, 256, 257, 1000, 5000, rng.randrange(1, 20000)]:
         counter, log = [0], {}
-        rc, g, tg = geometry(nd, nd_static)
+        rc, g, tg = geometry(nd, nd_static, consumers)
         tiles = -(-n_vec // tg)
         grid = min(rng.choice([1, 2, 5, 152]), tiles)
-        ctas = [Cta(nd, nd_static, n_vec, stages, counter, log) for _ in range(grid)]
+        ctas = [Cta(nd, nd_static, n_vec, stages, counter, log, consumers) for _ in range(grid)]
         live = list(ctas)
         while live:
             c = rng.choice(live)
