@@ -422,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, (ND >= 32) ? 5 : 0)
 // elements (TG = CONS when Nd is at least kRanks = 2048 / CONS). Its ranks are taken RC at a
 // time (RC = min(Nd, kRanks)), each chunk of RC ranks one 32 KiB stage of a kRbStages-stage
 // ring: RC bulk loads of the tile's slice of RC consecutive ranks, rank-major in the stage.
-// The producer claims tiles one at a time from the plan's counter (so CTAs on slower SMs
-// take fewer; the next claim is always in flight while a tile's loads are issued), waits
+// The producer claims tiles one at a time from the plan's counter, when it needs the next
+// one (so CTAs on slower SMs take fewer and no CTA holds a tile it has not started), waits
 // until a stage is empty, records the tile in it and issues the loads; after the last tile
 // it posts an end mark. Each consumer thread owns groups tid + CONS * j of the tile and
 // adds the chunks' ranks in order, so the sums are the same rank-order fp32 additions as
@@ -550,11 +550,9 @@ __global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
         *s_out = s;
         return true;
       };
-      // the claim of the next tile is issued before this tile's loads, so that its round
-      // trip overlaps them (a tile is a single stage when Nd <= 8)
-      long long t = (long long)atomicAdd(next_tile, 1ull);
-      for (; t < tiles; ) {
-        const long long t_after = (long long)atomicAdd(next_tile, 1ull);
+      for (;;) {
+        const long long t = (long long)atomicAdd(next_tile, 1ull);
+        if (t >= tiles) break;
         const long long v0 = t * TG;
         const long long nv = a.n_vec - v0 < TG ? a.n_vec - v0 : TG;
         const uint32_t bytes = (uint32_t)(nv * 16);
@@ -574,7 +572,6 @@ __global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
           ++q;
         }
         if (!ok) break;
-        t = t_after;
       }
       int s;
       if (ok && take_stage(&s)) {  // the end mark

@@ -1,8 +1,7 @@
 """CPU check of the bulk-load reduce's tile claiming and stage ring, restated.
 
 In each CTA a producer thread claims tiles of TG groups (groups of 8 elements) from a
-shared counter, the claim of the next tile made before the current tile's loads, and, for
-each tile, takes the ranks RC at a time (RC = min(Nd, 8); a
+shared counter when it needs the next one and, for each tile, takes the ranks RC at a time (RC = min(Nd, 8); a
 rank count known only at run time uses RC = 8 with a shorter last chunk). Each chunk is one
 stage of an S-stage ring: the producer waits until the stage's previous contents have
 been consumed, records (tile, chunk) in it and bulk-loads the chunk's ranks, rank-major,
@@ -59,12 +58,7 @@ class Cta:
         if self.q_prod >= self.S and self.empty[s] < self.q_prod // self.S:
             return False  # the stage's previous contents are not consumed yet
         if not self.pending:
-            # the claim of the tile after this one is made before this one's loads
-            if self.next_claim is None:
-                self.next_claim = self.claim()
-            t = self.next_claim
-            if t < self.tiles:
-                self.next_claim = self.claim()
+            t = self.claim()
             if t >= self.tiles:
                 self.stage[s] = ('end',)
                 self.full[s] += 1
