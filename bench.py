@@ -837,13 +837,17 @@ KERNEL_SOURCES = ("step_kernels.cu", "gather_kernel.cu", "bulk_async.h", "grid_s
 
 
 def kernel_source_hash() -> str:
-    """Short hash of the kernel sources; a committed traffic figure is used only if it was
-    captured on exactly these sources."""
+    """Short hash of the kernel sources' code (comments and whitespace removed); a
+    committed traffic figure is used only if it was captured on exactly this code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "sharded_emulated_reduce_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "sharded_emulated_reduce_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                  # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -27,10 +27,10 @@
  *     and owned by the caller; the library never frees it. "Device pointer" means an
  *     address the GPU can dereference: HBM, or pinned or registered host memory (on a
  *     GB300 the kernels then read and write it over NVLink-C2C, which is how optimizer
- *     state or fp16 shards can live in Grace memory — the offload variant of ZeRO). A plan owns only its host
- *     metadata, a small device scratch area (< 64 KiB, allocated by zero_plan_bind on
- *     the device current at that time, freed by zero_plan_destroy) and a few pinned
- *     host bytes.
+ *     state or fp16 shards can live in Grace memory — the offload variant of ZeRO). A
+ *     plan owns only its host metadata, a small device scratch area (< 64 KiB, allocated
+ *     by zero_plan_bind on the device current at that time, freed by zero_plan_destroy),
+ *     two CUDA streams with their events, and a few pinned host bytes.
  *   - Element types: fp16 buffers are IEEE binary16 (as torch.float16), fp32 buffers
  *     are IEEE binary32. All buffers are contiguous 1-D.
  *   - Streams are cudaStream_t passed as void*; NULL is the legacy default stream.
@@ -197,8 +197,9 @@ int zero_shard_reduce(zero_plan* plan, int32_t r0, int32_t r1, const void* const
  * zero_shard_reduce: word 0 counts non-finite summed gradients, words 1..4 hold the
  * exact sum of squares of (gsum * 2^24) as four 32-bit limbs (least significant first),
  * word 5 counts reduce CTAs whose bounded wait expired (0 on a healthy GPU; such a CTA also
- * adds a large count to word 0, so the step is skipped), words 6..7 are zero. Summing the buffers of all processes word by word (an integer
- * all-reduce) gives the statistics of the whole buffer. Valid after zero_plan_bind. */
+ * adds a large count to word 0, so the step is skipped), words 6..7 are zero. Summing the
+ * buffers of all processes word by word (an integer all-reduce) gives the statistics of the
+ * whole buffer. Valid after zero_plan_bind. */
 int zero_shard_stats(zero_plan* plan, void** dev_words);
 
 /* Second half of zero_shard_step: reads the (possibly all-reduced) exchange buffer,

@@ -63,7 +63,7 @@ struct DevScratch {
   unsigned int ticket;    // arrival counter of the reduce CTAs
   int32_t gather_status;  // 0, or kStatusGatherWait after a gather wait expired
   unsigned long long bar_arrivals;  // grid barrier of the fused small-span step (grows)
-  unsigned long long reduce_next;   // next tile the bulk-load reduce's CTAs claim (0 between launches)
+  unsigned long long reduce_next;   // next tile the bulk-load reduce claims (0 between launches)
   // tile counters of the bulk-copy gather: {next tile to claim, CTAs finished} per slot;
   // each launch takes the next slot of the ring, and its last CTA resets the slot to 0
   unsigned long long gather_sched[kGatherSlots][2];

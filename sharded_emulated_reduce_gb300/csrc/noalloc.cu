@@ -105,8 +105,8 @@ extern "C" int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // The ticket of the last-arriving CTA, the grid barrier's arrival count and the
-  // reduce's tile counter (which follow it) must start at zero; the step counter is the caller's and is copied in and out
-  // around the kernels.
+  // reduce's tile counter (which follow it) must start at zero; the step counter is the
+  // caller's and is copied in and out around the kernels.
   static_assert(offsetof(DevScratch, reduce_next) + sizeof(unsigned long long) -
                     offsetof(DevScratch, ticket) == 6 * sizeof(unsigned),
                 "ticket, gather status, the barrier's arrival count and the reduce's tile "
@@ -200,6 +200,7 @@ extern "C" int zero_noalloc_step_result(void* stream, zero_step_info* out) {
   out->bc1 = sc.bc1;
   out->bc2 = sc.bc2;
   out->loss_scale = sc.loss_scale;
-  if (sc.status != 0) return set_error(ZERO_EDEVICE, "the allocation-free step reported a device failure");
+  if (sc.status != 0)
+    return set_error(ZERO_EDEVICE, "the allocation-free step reported a device failure");
   return ZERO_OK;
 }

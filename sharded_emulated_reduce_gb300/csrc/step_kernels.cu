@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
   long long bad = 0;
   float s[G][8];
   long long q = 0;  // stages consumed
-  const int warp = tid >> 5, lane = tid & 31;
+  const int lane = tid & 31;
   for (;;) {
     const int si = (int)(q % kRbStages);
     if (!mbar_wait(&full[si], (uint32_t)((q / kRbStages) & 1))) {
@@ -650,7 +650,6 @@ __global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
       }
     }
   }
-  (void)warp;
 
   // CTA partial, then the last CTA to arrive combines all partials (no waiting)
   rb_block_reduce<CONS>(acc, bad);

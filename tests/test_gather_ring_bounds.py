@@ -1,8 +1,9 @@
 """CPU check of the gather's aligned-copy kernel: its tile claiming and ring, restated.
 
 The host cuts each layer at shard boundaries into segments and numbers fixed-size tiles
-across them (64 KiB; 32 KiB is checked too). In each CTA of the launch, thread 0 claims tiles from a shared counter (an
-atomic add), queues the ones with a 16-byte-aligned body, and streams the bodies, cut
+across them (32 KiB, the kernel's; 64 KiB is checked too). In each CTA of the launch,
+thread 0 claims tiles from a shared counter (an atomic add, one when it needs one), queues
+the ones with a 16-byte-aligned body, and streams the bodies, cut
 into chunks of at most 32 KiB, through a ring of S shared-memory buffers: it keeps S - 1
 loads in flight, stores chunk c from buffer c % S once it has landed, and issues the next
 load into a buffer only after waiting for every store but the newest to finish reading.
@@ -25,7 +26,7 @@ import random
 import numpy as np
 import pytest
 
-TILES = (32768, 16384)  # elements per tile (the kernel's, and a finer one)
+TILES = (16384, 32768)  # elements per tile (the kernel's 32 KiB, and 64 KiB)
 CHUNK = 32768           # bytes per ring buffer
 SHARD_BASE = 1 << 30    # synthetic byte addresses (16-byte aligned bases)
 LAYER_BASE = 1 << 50

@@ -72,3 +72,36 @@ def test_gather_from_shards_in_pinned_host_memory():
     for d, e in zip(dst, exp):
         assert np.array_equal(h16(d), e)
     plan.close()
+
+
+@pytest.mark.parametrize("nd", [4, 8, 64])
+def test_step_reads_gradients_from_pinned_host_memory(nd):
+    # the end-to-end bench's zero-copy mode: the gradient contributions stay in pinned
+    # Grace memory and the reduce reads them over NVLink-C2C (register loads for 4 ranks,
+    # TMA bulk loads for 8 and 64); the span is above the one-launch limit, so the reduce
+    # and update kernels run, and every element must match the oracle
+    n = 4_500_007 if nd <= 8 else 4_000_037
+    w = wl.Workload("hostgrads", cfg=520 + nd, n=n, nd=nd, align=8, stage=2, r0=0, r1=nd,
+                    loss_scale=1024.0, grad_sigma=1e-3, clip=1.0, steps=2, m_sigma=1e-3,
+                    v_sigma=1e-6)
+    first, n_span, n_valid = w.span()
+    master, m, v, p16, ws = wl.make_state(w)
+    om, omm, ov, op = f32(master).copy(), f32(m).copy(), f32(v).copy(), h16(p16).copy()
+    plan = z.zero_plan_create(w.n, w.nd, w.stage, w.align, w.hparams())
+    z.zero_plan_bind(plan, 0, w.nd, master, m, v, p16, ws, 0)
+    z.zero_profile_enable(plan, True)
+    t = 0
+    for step in range(w.steps):
+        host = [g.cpu().pin_memory() for g in wl.make_grads(w, step)]
+        z.zero_shard_step(plan, 0, w.nd, host, w.loss_scale, w.clip)
+        info = z.zero_step_result(plan)
+        sc = oracle.step([g.view(torch.int16).numpy().view(np.uint16) for g in host], om, omm,
+                         ov, op, w.loss_scale, w.clip, hyper(w), t, n_valid=n_valid)
+        assert_info_matches(info, sc)
+        t = sc.step
+    assert z.zero_profile_read(plan)[1][z.PROF_REDUCE] == w.steps  # the two-kernel path
+    assert np.array_equal(f32(master).view(np.uint32), om.view(np.uint32))
+    assert np.array_equal(f32(m).view(np.uint32), omm.view(np.uint32))
+    assert np.array_equal(f32(v).view(np.uint32), ov.view(np.uint32))
+    assert np.array_equal(h16(p16), op)
+    plan.close()

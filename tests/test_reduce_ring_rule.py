@@ -1,8 +1,9 @@
 """CPU check of the bulk-load reduce's tile claiming and stage ring, restated.
 
 In each CTA a producer thread claims tiles of TG groups (groups of 8 elements) from a
-shared counter when it needs the next one and, for each tile, takes the ranks RC at a time (RC = min(Nd, 8); a
-rank count known only at run time uses RC = 8 with a shorter last chunk). Each chunk is one
+shared counter when it needs the next one and, for each tile, takes the ranks RC at a time
+(RC = min(Nd, 2048 / consumers): 8 with 256 consumers, 4 with 512; a rank count known only
+at run time uses the full RC with a shorter last chunk). Each chunk is one
 stage of an S-stage ring: the producer waits until the stage's previous contents have
 been consumed, records (tile, chunk) in it and bulk-loads the chunk's ranks, rank-major,
 nv * 16 bytes each (nv = the tile's groups). Consumer thread c owns groups c + 256 j of

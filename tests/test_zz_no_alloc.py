@@ -8,8 +8,8 @@ inside the library. Here two calls in a row must leave the same state and step c
 as zero_shard_step on identical inputs, within the tolerances of the other parity tests
 (1e-6 relative for master/m/v, one fp16 ulp for the parameters), the companion
 zero_noalloc_step_result must report the step (no device failure, the same norm and
-counter), and a span longer than the array must be refused with a clear error. The test stands alone: it needs nothing
-from the tests collected before it.
+counter), and a span longer than the array must be refused with a clear error. The test
+stands alone: it needs nothing from the tests collected before it.
 """
 import numpy as np
 import pytest
