@@ -726,6 +726,14 @@ def run_ours(args, w0):
 
 E2E_LINK_GBS = 200.0  # host-to-device rate used only to size the end-to-end leg
 E2E_SECONDS = 3.0     # about this long per end-to-end mode
+E2E_HOST_SHARE = 0.4  # of the host's memory, split over the local processes
+
+
+def host_memory_bytes() -> int:
+    try:
+        return os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    except (ValueError, OSError, AttributeError):
+        return 0
 
 
 def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world,
@@ -742,9 +750,16 @@ def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world
     import torch
 
     import sharded_emulated_reduce_gb300 as z
-    host = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gsets[0]]
-    for h, g in zip(host, gsets[0]):
+    # one pinned buffer per logical rank while they fit the process's share of host memory;
+    # past it, the buffers are reused cyclically (every step still moves every rank's bytes)
+    per_rank = gsets[0][0].numel() * gsets[0][0].element_size()
+    local = max(1, env_int("LOCAL_WORLD_SIZE", 1))
+    budget = host_memory_bytes() * E2E_HOST_SHARE / local
+    distinct = len(gsets[0]) if budget <= 0 else max(1, min(len(gsets[0]), int(budget // per_rank)))
+    pinned = [torch.empty(g.numel(), dtype=g.dtype, pin_memory=True) for g in gsets[0][:distinct]]
+    for h, g in zip(pinned, gsets[0]):
         h.copy_(g)
+    host = [pinned[k % distinct] for k in range(len(gsets[0]))]
     dev_g = [[torch.empty_like(g) for g in gsets[0]] for _ in range(2)]
     p16_host = torch.empty(p16.numel(), dtype=p16.dtype, pin_memory=True)
     h2d_rank = sum(g.numel() * g.element_size() for g in gsets[0])
@@ -797,7 +812,7 @@ def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world
         run_mode(mode, steps)
         barrier()
         rates[mode] = total_params / job_max((time.perf_counter() - t0) / steps)
-    del host, dev_g
+    del host, pinned, dev_g
     with_params = rates.pop("copy_params_to_host")
     best = max(rates, key=rates.get)
     h2d = h2d_rank * world
@@ -805,6 +820,9 @@ def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world
     return {"value": rates[best], "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": STEP_INFO_D2H_BYTES * world, "steps": steps, "mode": best,
             "by_mode": rates,
+            "host_buffers": (f"{len(gsets[0])} distinct pinned gradient buffers" if distinct == len(gsets[0])
+                             else f"{distinct} distinct pinned buffers for {len(gsets[0])} ranks, reused "
+                                  f"cyclically (this process's share of host memory)"),
             "result_read_back": ("the step info (overflow flag, skip, norm, step counter) "
                                  "each step; the fp16 parameters stay in HBM, where the "
                                  "forward pass and the gather read them"),
