@@ -371,10 +371,11 @@ int zero_selftest_wait(uint32_t polls, int32_t* expired);
 
 /* Self-test of the grid barrier of the one-launch small-span step (a facility for failure
  * reporting; the pages have no counterpart): a cooperative launch of two CTAs meets at
- * the barrier with the given poll limit (1 .. 2^24 polls of about 64 ns). With skip_one
- * != 0 the second CTA leaves without arriving, so the first must give up; *expired is 1
- * if it gave up and 0 if the barrier was met. Synchronises the device. Errors:
- * ZERO_EINVAL, ZERO_ECUDA. */
+ * the barrier, which also sums values over the CTAs, with the given poll limit
+ * (1 .. 2^24 polls of about 64 ns). With skip_one != 0 the second CTA leaves without
+ * arriving, so the first must give up; *expired is 1 if it gave up, 0 if the barrier was
+ * met with the right sums and 2 if it was met with wrong ones. Synchronises the device.
+ * Errors: ZERO_EINVAL, ZERO_ECUDA. */
 int zero_selftest_grid_barrier(uint32_t polls, int32_t skip_one, int32_t* expired);
 
 /* Message of the calling thread's last error ("" if none). Valid until the thread's

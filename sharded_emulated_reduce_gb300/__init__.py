@@ -501,7 +501,8 @@ def zero_selftest_wait(polls: int = 4096) -> int:
 
 
 def zero_selftest_grid_barrier(polls: int = 4096, skip_one: bool = True) -> int:
-    """Run the grid-barrier self-test; 1 means the barrier gave up and reported it."""
+    """Run the grid-barrier self-test: 0 means it was met with the right sums, 1 that it
+    gave up and reported it, 2 that it was met with wrong sums."""
     out = _I32()
     _check(_lib.zero_selftest_grid_barrier(polls, 1 if skip_one else 0, ctypes.byref(out)))
     return out.value

@@ -12,6 +12,8 @@ constexpr int kThreads = 256;        // threads per CTA for every kernel
 constexpr int kMaxPartialBlocks = 1024;  // CTAs of the reduce kernel (one partial each)
 constexpr int kGatherSegs = 128;     // copy segments per gather launch
 constexpr int kGatherSlots = 64;     // tile-counter slots of the gather (a ring)
+constexpr int kSmallWords = 5;       // counting sums of the one-launch step (4 limbs, count)
+constexpr int kSumStride = 16;       // words from one counting sum to the next (128 bytes)
 
 // Scalars of one step, written by the finalize stage and read by the update kernel.
 struct DevScalars {
@@ -62,8 +64,12 @@ struct DevScratch {
   long long step;       // optimizer step counter t
   unsigned int ticket;    // arrival counter of the reduce CTAs
   int32_t gather_status;  // 0, or kStatusGatherWait after a gather wait expired
-  unsigned long long bar_arrivals;  // grid barrier of the fused small-span step (grows)
+  unsigned long long small_launch;  // launches of the one-launch step since the last reset
   unsigned long long reduce_next;   // next tile the bulk-load reduce claims (0 between launches)
+  // the one-launch step's counting sums (grid_sync.h), one set per launch parity: the
+  // four 32-bit limbs of the 128-bit sum of squares and the non-finite count, each word
+  // in its own 128-byte line; launch k uses set k & 1 and clears set (k + 1) & 1
+  alignas(128) unsigned long long small_sums[2][kSmallWords * kSumStride];
   // tile counters of the bulk-copy gather: {next tile to claim, CTAs finished} per slot;
   // each launch takes the next slot of the ring, and its last CTA resets the slot to 0
   unsigned long long gather_sched[kGatherSlots][2];

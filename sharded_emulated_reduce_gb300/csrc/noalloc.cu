@@ -104,14 +104,17 @@ extern "C" int zero_shard_step_noalloc(int32_t nd, int64_t n, int64_t n_valid,
   float* gsum = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kCtrlBytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // The ticket of the last-arriving CTA, the grid barrier's arrival count and the
-  // reduce's tile counter (which follow it) must start at zero; the step counter is the
-  // caller's and is copied in and out around the kernels.
-  static_assert(offsetof(DevScratch, reduce_next) + sizeof(unsigned long long) -
-                    offsetof(DevScratch, ticket) == 6 * sizeof(unsigned),
-                "ticket, gather status, the barrier's arrival count and the reduce's tile "
-                "counter are adjacent");
-  e = cudaMemsetAsync(&st->ticket, 0, 6 * sizeof(unsigned), s);
+  // The ticket of the last-arriving CTA, the one-launch step's launch count, the
+  // reduce's tile counter and the one-launch step's counting sums (which follow it in
+  // this order) must start at zero; the step counter is the caller's and is copied in and
+  // out around the kernels.
+  constexpr size_t first = offsetof(DevScratch, ticket);
+  constexpr size_t end = offsetof(DevScratch, small_sums) + sizeof(DevScratch::small_sums);
+  static_assert(offsetof(DevScratch, small_launch) > first &&
+                    offsetof(DevScratch, reduce_next) > first &&
+                    offsetof(DevScratch, small_sums) > first,
+                "the counters follow the ticket");
+  e = cudaMemsetAsync(reinterpret_cast<unsigned char*>(st) + first, 0, end - first, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(&st->step, step_counter, sizeof(int64_t), cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return bad(ZERO_ECUDA, "scratch set-up copy failed");

@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -619,9 +620,12 @@ int zero_step_result(zero_plan* p, zero_step_info* out) {
   out->bc2 = sc.bc2;
   out->loss_scale = sc.loss_scale;
   if (sc.status == zero::kStatusStepWait) {
-    // the fused step's grid barrier gave up: its arrival count may be left part-way, so
-    // start the next one from zero
-    cudaMemsetAsync(&p->scratch->bar_arrivals, 0, sizeof(unsigned long long), p->last_stream);
+    // the one-launch step's wait gave up: start its launch count and counting sums (and
+    // the reduce's tile counter between them, zero between launches) from zero
+    constexpr size_t first = offsetof(zero::DevScratch, small_launch);
+    constexpr size_t end = offsetof(zero::DevScratch, small_sums) + sizeof(zero::DevScratch::small_sums);
+    cudaMemsetAsync(reinterpret_cast<unsigned char*>(p->scratch) + first, 0, end - first,
+                    p->last_stream);
     cudaStreamSynchronize(p->last_stream);
   }
   if (sc.status != 0) return fail(ZERO_EDEVICE, "device status %d", sc.status);

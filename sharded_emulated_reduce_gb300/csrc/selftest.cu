@@ -5,9 +5,10 @@
 // kernel must record that and return, and the context must stay usable. This exercises
 // the failure path of the bulk-copy kernels without faulting, trapping or hanging the GPU.
 //
-// zero_selftest_grid_barrier: a cooperative launch of two CTAs meets at the grid barrier
-// of the one-launch step; with skip_one set, CTA 1 leaves without arriving, so CTA 0's
-// wait must give up within its poll limit and record that.
+// zero_selftest_grid_barrier: a cooperative launch of two CTAs meets at the counting sums
+// that are the one-launch step's grid barrier, each adding two values; CTA 0 checks the
+// two sums. With skip_one set, CTA 1 leaves without adding, so CTA 0's wait must give up
+// within its poll limit and record that.
 #include "bulk_async.h"
 #include "grid_sync.h"
 #include "internal.h"
@@ -26,17 +27,25 @@ __global__ void k_wait_probe(unsigned polls, int32_t* out) {
   if (threadIdx.x == 0) *out = arrived ? 0 : 1;
 }
 
-__global__ void k_barrier_probe(unsigned polls, int skip_one, unsigned long long* arrivals,
+// One warp per CTA; *out = 0 if the sums were met and right, 1 if the wait gave up, 2 if
+// they were met but wrong.
+__global__ void k_barrier_probe(unsigned polls, int skip_one, unsigned long long* words,
                                 int32_t* out) {
-  if (threadIdx.x != 0) return;
   if (skip_one && blockIdx.x == 1) return;  // never arrives
-  const bool met = grid_barrier(arrivals, gridDim.x, polls);
-  if (blockIdx.x == 0) *out = met ? 0 : 1;
+  if (threadIdx.x == 0) {
+    const unsigned long long v[2] = {blockIdx.x + 1ull, 100ull + blockIdx.x};
+    sum_arrive<2>(words, kSumStride, v);
+  }
+  unsigned long long sum = 0;
+  const bool met = sum_wait<2>(words, kSumStride, gridDim.x, polls, &sum);
+  const unsigned long long s0 = __shfl_sync(0xffffffffu, sum, 0);
+  const unsigned long long s1 = __shfl_sync(0xffffffffu, sum, 1);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *out = !met ? 1 : (s0 == 3 && s1 == 201) ? 0 : 2;
 }
 
 // Result word of the probe; host code gets its device address from cudaGetSymbolAddress.
 static __device__ int32_t g_probe_result;
-static __device__ unsigned long long g_probe_barrier;
+static __device__ unsigned long long g_probe_words[2 * kSumStride];
 
 }  // namespace
 }  // namespace zero
@@ -67,9 +76,9 @@ extern "C" int zero_selftest_grid_barrier(uint32_t polls, int32_t skip_one, int3
   void* res = nullptr;
   void* words = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&res, g_probe_result);
-  if (e == cudaSuccess) e = cudaGetSymbolAddress(&words, g_probe_barrier);
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(&words, g_probe_words);
   if (e == cudaSuccess) e = cudaMemset(res, 0xff, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMemset(words, 0, sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(words, 0, sizeof(unsigned long long) * 2 * kSumStride);
   if (e != cudaSuccess) return set_error(ZERO_ECUDA, "self-test set-up failed");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);

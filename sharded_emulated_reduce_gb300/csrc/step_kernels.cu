@@ -121,6 +121,29 @@ __device__ __noinline__ DevPre pre_scalars_call(long long t, const HostHParams& 
   return pre_scalars(t, hp);
 }
 
+// The same with the two powers computed side by side, by lanes 0 and 1 of the calling
+// warp, in about half the time of one after the other (every lane calls it; the result
+// is valid in lane 0).
+__device__ __noinline__ DevPre pre_scalars_warp(long long t, const HostHParams& hp) {
+  const int lane = threadIdx.x & 31;
+  const double tp = (double)(t + 1);
+  const double pw = pow(lane == 1 ? (double)hp.beta2 : (double)hp.beta1, tp);
+  const double pw2 = __shfl_sync(0xffffffffu, pw, 1);
+  DevPre p;
+  p.omb1 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta1));
+  p.omb2 = __double2float_rn(__dadd_rn(1.0, -(double)hp.beta2));
+  p.bc1 = __double2float_rn(__dadd_rn(1.0, -pw));
+  p.bc2 = __double2float_rn(__dadd_rn(1.0, -pw2));
+  p.decay = __double2float_rn(__dadd_rn(1.0, -__dmul_rn((double)hp.lr, (double)hp.weight_decay)));
+  p.lr = hp.lr;
+  p.beta1 = hp.beta1;
+  p.beta2 = hp.beta2;
+  p.weight_decay = hp.weight_decay;
+  p.valid = kPreValid;
+  p.t = t;
+  return p;
+}
+
 static_assert(sizeof(DevPre) == 48, "a slot is three 16-byte vectors");
 
 // Slot `p` read through L2 in one round trip (three independent 16-byte loads).
@@ -174,7 +197,11 @@ __device__ __forceinline__ double div_by_loss_scale(double x, float L) {
 
 // The step's scalars from its statistics (one thread), writing nothing: t and `scaler`
 // are the step counter and loss scaler before the step, *next the scaler after it.
-// Double arithmetic, each operation rounded to nearest, then one rounding to fp32.
+// Double arithmetic, each operation rounded to nearest, then one rounding to fp32. With
+// REPORT false only what the update reads is exact: the sum of squares and the norm (a
+// square root, and a long dependent chain of double operations on this part) are then
+// computed only when clipping needs them, and are 0 otherwise.
+template <bool REPORT = true>
 __device__ __forceinline__ DevScalars make_scalars(long long t, DevScaler scaler, long long bad,
                                                    U128 ss, float loss_scale_arg, float clip,
                                                    const HostHParams& hp, const DevPre& pre,
@@ -187,15 +214,16 @@ __device__ __forceinline__ DevScalars make_scalars(long long t, DevScaler scaler
   sc.pad2 = 0.0f;
   sc.pad = 0;
   sc.status = 0;
-  sc.ss = __dmul_rn(u128_to_double(ss), 0x1p-48);
   sc.overflow = bad > 0 ? 1 : 0;
   sc.skipped = sc.overflow;
+  const bool norm_needed = REPORT || (!sc.overflow && clip > 0.0f);
+  sc.ss = norm_needed ? __dmul_rn(u128_to_double(ss), 0x1p-48) : 0.0;
   if (sc.overflow) {
     sc.norm = __longlong_as_double(0x7ff0000000000000ll);  // +inf
     sc.clip_coef = 1.0;
     sc.step = t;
   } else {
-    sc.norm = div_by_loss_scale(__dsqrt_rn(sc.ss), loss_scale);
+    sc.norm = norm_needed ? div_by_loss_scale(__dsqrt_rn(sc.ss), loss_scale) : 0.0;
     double coef = 1.0;
     if (clip > 0.0f) {
       const double c = __ddiv_rn((double)clip, __dadd_rn(sc.norm, 1e-6));
@@ -892,20 +920,22 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
 // A span of at most kWideVecs groups of 8 per SM runs as one cooperative launch (all
 // CTAs resident at once), one 512-thread CTA per SM, each owning a contiguous slice:
 //   1. the CTA sums its slice of the contributions in rank order into shared memory and
-//      publishes its 128-bit sum of squares and non-finite count;
-//   2. after a grid-wide barrier (bounded: it gives up after about kWaitNs and records
-//      kStatusStepWait), warp 0 of every CTA combines all the partials, the same
-//      integers in the same order, so every CTA derives the same scalars; CTA 0 commits
-//      them (and the step counter and scaler) to the scratch;
+//      adds its 128-bit sum of squares (as four 32-bit limbs) and non-finite count to the
+//      launch's counting sums (grid_sync.h);
+//   2. warp 0 of every CTA waits until those count every CTA (the grid-wide barrier;
+//      bounded: it gives up after about kWaitNs and records kStatusStepWait) and reads
+//      the exact totals in the same round trip, so every CTA derives the same scalars;
 //   3. unless the step is skipped, the CTA updates its slice from the sums it kept.
 // The fp32 sums never go to HBM and the step is one launch. A slice of at most
 // kSmallVecs groups also has its master/m/v brought into shared memory by bulk loads
-// issued once the CTA has arrived at the grid barrier, so they arrive while the CTAs wait
-// there and derive the scalars (DRAM is otherwise idle then); a longer slice reads them
-// from global memory in the update. A 17th warp of CTA 0
-// prepares the next step's t-only scalars meanwhile; it reads the step counter before
-// CTA 0 may advance it (named barrier 2), and the CTAs' own synchronisation uses named
-// barrier 1 over the 512 working threads only.
+// issued once the CTA has added its statistics, so they arrive while the CTAs wait and
+// derive the scalars (DRAM is otherwise idle then); a longer slice reads them from global
+// memory in the update. A 17th warp of CTA 0 prepares the next step's t-only
+// scalars, then takes the totals from warp 0 (named barrier 2) and commits the step's
+// statistics, scalars, step counter and scaler to the scratch while the CTAs update: so
+// the update waits for the norm's square root and divisions only when clipping is on
+// (the scale the update applies depends on the norm only then). The CTAs' own
+// synchronisation uses named barrier 1 over the 512 working threads only.
 constexpr int kSmallThreads = 512;
 constexpr int kSmallVecs = 1024;  // groups of 8 per CTA whose state is prefetched
 constexpr int kWideVecs = 3072;   // groups of 8 per CTA at most (96 KiB of fp32 sums)
@@ -957,6 +987,46 @@ __device__ void small_block_reduce(U128& acc, long long& bad) {
   }
 }
 
+// The step's statistics, scalars, step counter and loss scaler committed to the scratch
+// (one thread of CTA 0, once every CTA has added its statistics): every scalar field
+// but the status word, which a CTA whose barrier expired may set.
+template <int CAP>
+__device__ __noinline__ void commit_small(DevScratch* st, long long t, DevScaler scaler,
+                                          DevPre pre, long long tb, U128 tot,
+                                          const ReduceArgs<CAP>& r) {
+  if (!pre_matches(pre, t, r.hp)) pre = pre_scalars_call(t, r.hp);
+  DevScaler next;
+  const DevScalars sc = make_scalars(t, scaler, tb, tot, r.loss_scale, r.clip, r.hp, pre, &next);
+  st->stats[0] = tb;
+  st->stats[1] = (long long)(tot.lo & 0xffffffffull);
+  st->stats[2] = (long long)(tot.lo >> 32);
+  st->stats[3] = (long long)(tot.hi & 0xffffffffull);
+  st->stats[4] = (long long)(tot.hi >> 32);
+  st->stats[5] = st->stats[6] = st->stats[7] = 0;
+  DevScalars* d = &st->sc;
+  d->overflow = sc.overflow;
+  d->skipped = sc.skipped;
+  d->pad = sc.pad;
+  d->step = sc.step;
+  d->ss = sc.ss;
+  d->norm = sc.norm;
+  d->clip_coef = sc.clip_coef;
+  d->s = sc.s;
+  d->omb1 = sc.omb1;
+  d->omb2 = sc.omb2;
+  d->bc1 = sc.bc1;
+  d->bc2 = sc.bc2;
+  d->decay = sc.decay;
+  d->lr = sc.lr;
+  d->beta1 = sc.beta1;
+  d->beta2 = sc.beta2;
+  d->eps = sc.eps;
+  d->loss_scale = sc.loss_scale;
+  d->pad2 = sc.pad2;
+  if (!sc.skipped) st->step = t + 1;
+  if (scaler.interval > 0) st->scaler = next;
+}
+
 template <int ND, int CAP>
 __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     k_step_small(const __grid_constant__ SmallArgs<CAP> a) {
@@ -971,16 +1041,26 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   __shared__ DevScaler s_scaler;
   __shared__ DevPre s_pre;
   __shared__ int s_ok;
+  __shared__ U128 s_tot;
+  __shared__ long long s_tb;
+  __shared__ unsigned long long s_k;  // this launch's number (its counting sums: set s_k & 1)
   DevScratch* st = a.r.st;
   const int tid = threadIdx.x;
   if (tid >= kSmallThreads) {  // the 17th warp
     if (blockIdx.x == 0) {
+      // the next step's t-only scalars, off the critical path: the two powers take about
+      // as long as the rest of the step
       const long long tn = st->step + 1;  // the counter after an applied step
-      bar_arrive(2, 64);                  // CTA 0's commit waits for this read
-      if (tid == kSmallThreads) {
-        DevPre* slot = &st->pre[tn & 1];
-        if (!pre_matches(load_pre(slot), tn, a.r.hp)) *slot = pre_scalars_call(tn, a.r.hp);
+      DevPre* slot = &st->pre[tn & 1];
+      const bool have = __shfl_sync(0xffffffffu, pre_matches(load_pre(slot), tn, a.r.hp), 0);
+      if (!have) {
+        const DevPre p = pre_scalars_warp(tn, a.r.hp);
+        if (tid == kSmallThreads) *slot = p;
       }
+      // warp 0 has waited for the counting sums (s_ok) and, if they completed, has the totals
+      __syncwarp();
+      bar_sync(2, 64);
+      if (tid == kSmallThreads && s_ok) commit_small(st, s_t, s_scaler, s_pre, s_tb, s_tot, a.r);
     }
     return;
   }
@@ -1001,15 +1081,25 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     // this step's t-only scalars, read while the CTA reduces (slot t & 1; this launch
     // writes only slot (t + 1) & 1)
     s_pre = load_pre(&st->pre[s_t & 1]);
-    if (blockIdx.x == 0) st->sc.status = 0;
+    // read before this CTA adds to the counting sums (their address depends on it), so
+    // before CTA 0 advances it once every CTA has added
+    s_k = st->small_launch;
+    if (blockIdx.x == 0) {
+      st->sc.status = 0;
+      // the next launch's counting sums start from zero (the previous launch, which used
+      // them, has ended)
+      unsigned long long* next = st->small_sums[(s_k + 1) & 1];
+#pragma unroll
+      for (int j = 0; j < kSmallWords; ++j) next[j * kSumStride] = 0;
+    }
     if (state_bytes > 0) {
       mbar_init(state_bar, 1);
       mbar_fence_init();
     }
   }
-  // the slice's state is brought in by bulk loads issued once this CTA has arrived at the
-  // grid barrier (so that they compete neither with the reduce's loads nor with the
-  // barrier's own atomics); it arrives while the CTAs wait there and derive the scalars
+  // the slice's state is brought in by bulk loads issued once this CTA has added its
+  // statistics (so that they compete neither with the reduce's loads nor with the
+  // counting sums' atomics); it arrives while the CTAs wait and derive the scalars
   auto issue_state_loads = [&]() {
     if (tid == 0 && state_bytes > 0) {
       mbar_expect_tx(state_bar, 3 * state_bytes);
@@ -1044,11 +1134,48 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     finish(v, s0);
   }
   small_block_reduce(acc, bad);
+
+  // 2. the CTAs' statistics summed by the counting sums, which are also the grid barrier
+  //    (bounded: the wait gives up after about kWaitNs and records kStatusStepWait); every
+  //    CTA gets the same exact totals and derives the same scalars for its update
+  unsigned long long* counting = st->small_sums[s_k & 1];
   if (tid == 0) {
-    st->partials[blockIdx.x].lo = acc.lo;
-    st->partials[blockIdx.x].hi = acc.hi;
-    st->partials[blockIdx.x].bad = bad;
-    s_ok = grid_barrier(&st->bar_arrivals, gridDim.x, kBarrierPolls, issue_state_loads) ? 1 : 0;
+    const unsigned long long v[kSmallWords] = {acc.lo & 0xffffffffull, acc.lo >> 32,
+                                               acc.hi & 0xffffffffull, acc.hi >> 32,
+                                               (unsigned long long)bad};
+    sum_arrive<kSmallWords>(counting, kSumStride, v);
+    issue_state_loads();
+  }
+  if (tid < 32) {
+    unsigned long long w = 0;
+    const bool met = sum_wait<kSmallWords>(counting, kSumStride, gridDim.x, kBarrierPolls, &w);
+    // met: every CTA has added its partial; lane j holds the sum of word j
+    const unsigned long long l0 = __shfl_sync(0xffffffffu, w, 0);
+    const unsigned long long l1 = __shfl_sync(0xffffffffu, w, 1);
+    const unsigned long long l2 = __shfl_sync(0xffffffffu, w, 2);
+    const unsigned long long l3 = __shfl_sync(0xffffffffu, w, 3);
+    const long long tb = (long long)__shfl_sync(0xffffffffu, w, 4);
+    U128 tot{l0, 0};  // l0 + l1 2^32 + l2 2^64 + l3 2^96 (each limb sum < 2^48)
+    add128(tot, l1 << 32, l1 >> 32);
+    add128(tot, 0, l2);
+    add128(tot, 0, l3 << 32);
+    if (tid == 0) s_ok = met ? 1 : 0;
+    if (blockIdx.x == 0) {  // the totals to the 17th warp, which commits the step
+      if (tid == 0) {
+        st->small_launch = s_k + 1;
+        s_tot = tot;
+        s_tb = tb;
+      }
+      __syncwarp();
+      bar_arrive(2, 64);
+    }
+    if (met && tid == 0) {  // what the update needs, with the norm only if clipping uses it
+      DevPre pre = s_pre;
+      if (!pre_matches(pre, s_t, a.r.hp)) pre = pre_scalars_call(s_t, a.r.hp);
+      DevScaler next;
+      s_sc = make_scalars<false>(s_t, s_scaler, tb, tot, a.r.loss_scale, a.r.clip, a.r.hp, pre,
+                                 &next);
+    }
   }
   bar_sync(1, kSmallThreads);
   if (!s_ok) {
@@ -1056,84 +1183,6 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
     drain();
     return;
   }
-
-  // 2. every CTA: the same combine and the same scalars; CTA 0 commits them
-  if (tid < 32) {
-    U128 tot{0, 0};
-    long long tb = 0;
-    // a lane's partials are all loaded before any is added: one round trip to L2 per
-    // pass of 32 * kPer partials (one pass for up to 256 SMs)
-    constexpr int kPer = 8;
-    for (int base = 0; base < (int)gridDim.x; base += 32 * kPer) {
-      longlong2 w[kPer][2];
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = base + tid + 32 * k;
-        if (i < (int)gridDim.x) {
-          const longlong2* q = reinterpret_cast<const longlong2*>(&st->partials[i]);
-          w[k][0] = __ldcg(q);
-          w[k][1] = __ldcg(q + 1);
-        } else {
-          w[k][0] = w[k][1] = make_longlong2(0, 0);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        add128(tot, (unsigned long long)w[k][0].x, (unsigned long long)w[k][0].y);
-        tb += w[k][1].x;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long lo = __shfl_xor_sync(0xffffffffu, tot.lo, o);
-      const unsigned long long hi = __shfl_xor_sync(0xffffffffu, tot.hi, o);
-      tb += __shfl_xor_sync(0xffffffffu, tb, o);
-      add128(tot, lo, hi);
-    }
-    DevScaler next;
-    DevScalars sc;
-    if (tid == 0) {
-      DevPre pre = s_pre;
-      if (!pre_matches(pre, s_t, a.r.hp)) pre = pre_scalars_call(s_t, a.r.hp);
-      sc = make_scalars(s_t, s_scaler, tb, tot, a.r.loss_scale, a.r.clip, a.r.hp, pre, &next);
-      s_sc = sc;
-    }
-    if (blockIdx.x == 0) {
-      bar_sync(2, 64);  // the 17th warp has read the step counter
-      if (tid == 0) {
-        st->stats[0] = tb;
-        st->stats[1] = (long long)(tot.lo & 0xffffffffull);
-        st->stats[2] = (long long)(tot.lo >> 32);
-        st->stats[3] = (long long)(tot.hi & 0xffffffffull);
-        st->stats[4] = (long long)(tot.hi >> 32);
-        st->stats[5] = st->stats[6] = st->stats[7] = 0;
-        // every field but the status word, which a CTA whose barrier expired may set
-        DevScalars* d = &st->sc;
-        d->overflow = sc.overflow;
-        d->skipped = sc.skipped;
-        d->pad = sc.pad;
-        d->step = sc.step;
-        d->ss = sc.ss;
-        d->norm = sc.norm;
-        d->clip_coef = sc.clip_coef;
-        d->s = sc.s;
-        d->omb1 = sc.omb1;
-        d->omb2 = sc.omb2;
-        d->bc1 = sc.bc1;
-        d->bc2 = sc.bc2;
-        d->decay = sc.decay;
-        d->lr = sc.lr;
-        d->beta1 = sc.beta1;
-        d->beta2 = sc.beta2;
-        d->eps = sc.eps;
-        d->loss_scale = sc.loss_scale;
-        d->pad2 = sc.pad2;
-        if (!sc.skipped) st->step = s_t + 1;
-        if (s_scaler.interval > 0) st->scaler = next;
-      }
-    }
-  }
-  bar_sync(1, kSmallThreads);
 
   // 3. the update of this CTA's slice from the sums and state it holds
   if (s_sc.skipped) {  // overflow: the state keeps its bits
