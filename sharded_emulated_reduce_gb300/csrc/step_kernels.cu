@@ -164,6 +164,15 @@ __device__ __forceinline__ bool pre_matches(const DevPre& p, long long t, const 
          p.beta2 == hp.beta2 && p.weight_decay == hp.weight_decay;
 }
 
+// The t-only scalars of step counter t into slot t & 1, unless the slot holds them
+// already; every lane of the calling warp calls it (the two powers run side by side).
+__device__ __forceinline__ void fill_pre_slot(DevScratch* st, long long t, const HostHParams& hp) {
+  DevPre* slot = &st->pre[t & 1];
+  if (__shfl_sync(0xffffffffu, pre_matches(load_pre(slot), t, hp) ? 1 : 0, 0)) return;
+  const DevPre p = pre_scalars_warp(t, hp);
+  if ((threadIdx.x & 31) == 0) *slot = p;
+}
+
 // The t-only scalars for step counter t: from slot t & 1 when its tag matches, otherwise
 // computed here, inline with INLINE (the full-wave reduce, whose code generation is tuned
 // with it) or as a call.
@@ -366,11 +375,7 @@ __global__ void __launch_bounds__(kThreads, (ND >= 32) ? 5 : 0)
   DevScratch* st = a.st;
   if constexpr (PRE) {
     if (blockIdx.x == 0) {
-      if (threadIdx.x == 0) {
-        const long long tn = st->step + 1;
-        DevPre* slot = &st->pre[tn & 1];
-        if (!pre_matches(load_pre(slot), tn, a.hp)) *slot = pre_scalars_call(tn, a.hp);
-      }
+      if (threadIdx.x < 32) fill_pre_slot(st, st->step + 1, a.hp);
       return;
     }
   }
@@ -541,11 +546,7 @@ __global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
   const int tid = threadIdx.x;
   if constexpr (PRE) {
     if (blockIdx.x == 0) {  // no reduce work: the next step's t-only scalars
-      if (tid == 0) {
-        const long long tn = st->step + 1;
-        DevPre* slot = &st->pre[tn & 1];
-        if (!pre_matches(load_pre(slot), tn, a.hp)) *slot = pre_scalars_call(tn, a.hp);
-      }
+      if (tid < 32) fill_pre_slot(st, st->step + 1, a.hp);
       return;
     }
   }
@@ -747,10 +748,8 @@ __global__ void k_finalize(DevScratch* st, float loss_scale, float clip, HostHPa
 // The t-only scalars for the counter now in the scratch (the next step's), off the
 // step's critical path: launched on a second stream while the update runs.
 __global__ void k_next_scalars(DevScratch* st, HostHParams hp) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  const long long t = st->step;
-  DevPre* slot = &st->pre[t & 1];
-  if (!pre_matches(load_pre(slot), t, hp)) *slot = pre_scalars_call(t, hp);
+  if (blockIdx.x != 0 || threadIdx.x >= 32) return;
+  fill_pre_slot(st, st->step, hp);
 }
 
 struct UpdateArgs {
@@ -1048,15 +1047,9 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   const int tid = threadIdx.x;
   if (tid >= kSmallThreads) {  // the 17th warp
     if (blockIdx.x == 0) {
-      // the next step's t-only scalars, off the critical path: the two powers take about
-      // as long as the rest of the step
-      const long long tn = st->step + 1;  // the counter after an applied step
-      DevPre* slot = &st->pre[tn & 1];
-      const bool have = __shfl_sync(0xffffffffu, pre_matches(load_pre(slot), tn, a.r.hp), 0);
-      if (!have) {
-        const DevPre p = pre_scalars_warp(tn, a.r.hp);
-        if (tid == kSmallThreads) *slot = p;
-      }
+      // the next step's t-only scalars (for the counter after an applied step), off the
+      // critical path: the two powers take about half as long as the rest of the step
+      fill_pre_slot(st, st->step + 1, a.r.hp);
       // warp 0 has waited for the counting sums (s_ok) and, if they completed, has the totals
       __syncwarp();
       bar_sync(2, 64);
