@@ -72,6 +72,23 @@ def test_overflow_injection(where, rank, value):
     assert r.exact
 
 
+@pytest.mark.parametrize("where", ["first", "last"])
+@pytest.mark.parametrize("ls", [1024.0, 3.0])
+def test_clip_off_overflow_and_applied_steps_in_one_launch(where, ls):
+    # clipping off (the update's scale is then 1 / loss scale and needs no norm) in the
+    # one-launch step: the overflow at step 1 must leave every state bit as it was, and
+    # the applied steps must match the oracle
+    n = 1_000_003
+    idx = 0 if where == "first" else n - 1
+    w = small(n=n, clip=0.0, loss_scale=ls, steps=3, cfg=157,
+              inject=((1, 3, wl.POS_INF, idx),))
+    r = Runner(w).run()
+    assert [x["skipped"] for x in r.results] == [0, 1, 0]
+    assert [x["step"] for x in r.results] == [1, 1, 2]
+    assert all(x["clip_coef"] == 1.0 for x in r.results)
+    assert r.exact
+
+
 def test_opposite_infinities_in_two_ranks_make_nan_and_skip():
     w = small(n=3000, nd=4, steps=2, cfg=160,
               inject=((0, 0, wl.POS_INF, 1234), (0, 3, wl.NEG_INF, 1234)))
