@@ -34,8 +34,8 @@ struct DevScaler {
   int32_t pad;
 };
 
-// One reduce CTA's statistics: the 128-bit sum of squares and the non-finite count
-// (16-byte aligned: the one-launch step reads each as two 16-byte vectors).
+// One reduce CTA's statistics: the 128-bit sum of squares and the non-finite count, which
+// the last CTA of the reduce kernels combines.
 struct alignas(16) DevPartial {
   unsigned long long lo, hi;
   long long bad;
