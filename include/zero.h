@@ -311,7 +311,7 @@ int zero_profile_read(zero_plan* plan, double* ms, int64_t* launches, int32_t re
  *     and written after the step (it stays unchanged when the step is skipped);
  *   hp, loss_scale, clip: as for zero_plan_create and zero_shard_step.
  * The caller passes every input and output. Scratch comes from one device array inside
- * this library: ZERO_NOALLOC_MAX_SPAN fp32 values plus a control block of about 34 KiB
+ * this library: ZERO_NOALLOC_MAX_SPAN fp32 values plus a control block of about 35 KiB
  * (16.03 MiB), which every GPU that loads the library holds until the process exits. The
  * first call on a device looks up that array's device address (cudaGetSymbolAddress) and
  * caches it; make that first call before any stream capture. Every call shares the array

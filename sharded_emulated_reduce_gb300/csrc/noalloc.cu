@@ -9,7 +9,7 @@
 // scalars) from one file-scope device array instead of from a plan.
 //
 // The array is kNoallocSpanMax fp32 values plus the small control block: 16 MiB +
-// ~34 KiB. Every GPU that loads this library holds it until the process exits. All calls
+// ~35 KiB. Every GPU that loads this library holds it until the process exits. All calls
 // share it, and it keeps the last call's contents, so two calls whose work overlaps on
 // the GPU (different streams, or different host threads, without ordering between them)
 // race on it and produce wrong results.
