@@ -478,8 +478,11 @@ def run_ours(args, w0):
     dist = None
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        # one process per GPU; a rehearsal of the multi-process path with more processes
+        # than GPUs (ZERO_BENCH_BACKEND=gloo: host-side collectives only, no kernel waits
+        # on another process) shares them round robin
+        torch.cuda.set_device(local % torch.cuda.device_count())
+        dist.init_process_group(os.environ.get("ZERO_BENCH_BACKEND", "nccl"))
     else:
         torch.cuda.set_device(0)
     w, scaling = process_span(w0, world, rank)
