@@ -125,3 +125,27 @@ def test_two_processes_split_the_span_bit_identically(n):
             x_bits = x.view(np.uint32) if x.dtype == np.float32 else x
             y_bits = y[sl].view(np.uint32) if y.dtype == np.float32 else y[sl]
             assert np.array_equal(x_bits, y_bits), rank
+
+
+def test_bench_line_from_two_processes():
+    # the bench's multi-process path (process group, barriers, max over processes, rank
+    # 0's single line), rehearsed with two processes sharing the one GPU over gloo: the
+    # 1M workload's four logical ranks split over the two (strong scaling)
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, ZERO_BENCH_BACKEND="gloo")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), "bench.py",
+           "--gpus", "2", "--workload", "zero2_tiny_1m_nd4", "--steps", "5", "--warmup", "3",
+           "--cpu-seconds", "0"]
+    out = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["scaling"] == "strong" and d["value"] > 0
+    assert d["config"]["workload"] == "zero2_tiny_1m_nd4"
+    assert d["e2e"]["value"] > 0 and d["gather"]["value"] > 0
+    assert d["last_step"]["skipped"] == 0
