@@ -89,6 +89,23 @@ def test_clip_off_overflow_and_applied_steps_in_one_launch(where, ls):
     assert r.exact
 
 
+@pytest.mark.parametrize("path", ["one launch", "two kernels"])
+def test_many_steps_stay_bit_exact(path):
+    # hundreds of consecutive steps (the launch counts and scalar slots cycling, the bias
+    # corrections at large t), two of them skipped by injected overflows: every element
+    # of every output equals the oracle's, bit for bit, at every step
+    if path == "one launch":
+        w = dataclasses.replace(TINY, name="tiny_long", steps=1000,
+                                inject=((57, 1, wl.POS_INF, 123), (211, 3, wl.QNAN, 777_777)))
+    else:
+        w = small(n=5_000_003, steps=200, cfg=158,
+                  inject=((17, 0, wl.NEG_INF, 4_999_999), (64, 2, wl.POS_INF, 2_500_000)))
+    r = Runner(w, mode="full_parallel").run()
+    assert sum(x["skipped"] for x in r.results) == 2
+    assert r.results[-1]["step"] == w.steps - 2
+    assert r.exact
+
+
 def test_opposite_infinities_in_two_ranks_make_nan_and_skip():
     w = small(n=3000, nd=4, steps=2, cfg=160,
               inject=((0, 0, wl.POS_INF, 1234), (0, 3, wl.NEG_INF, 1234)))
