@@ -431,6 +431,48 @@ def config_of(w, n_gpus):
             "state": "HBM"}
 
 
+def append_results(path, records) -> None:
+    """Append one JSON record per line to `path` (the per-kernel results log)."""
+    stamp = time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime())
+    with open(path, "a") as f:
+        for r in records:
+            f.write(json.dumps(dict(r, time=stamp)) + "\n")
+
+
+def kernel_records(line, kinds, kms, klaunch, w, traffic_of) -> list:
+    """The results-log records of one GPU bench line: one per kernel (its algorithmic and
+    moved GB/s and fraction of peak), the whole step, and the gather if it ran."""
+    peak = line["roofline"]["peak"]
+    base = {"workload": line["config"]["workload"], "impl": "ours", "n_gpus": line["n_gpus"],
+            "peak_gbs": peak}
+    cpu = line.get("cpu_baseline") or {}
+    span_params = line["config"]["params_in_span"]
+    out = []
+    for k, (name, alg) in kinds.items():
+        if not klaunch[k]:
+            continue
+        ms = kms[k] / klaunch[k]
+        traffic = traffic_of(name)
+        out.append(dict(base, kernel=name, launches=int(klaunch[k]), avg_ms=ms,
+                        alg_bytes_per_launch=alg, alg_gbs=alg / ms / 1e6,
+                        frac_of_peak=alg / ms / 1e6 / peak,
+                        moved_bytes_per_launch=traffic,
+                        moved_gbs=None if traffic is None else traffic / ms / 1e6))
+    h = line["step_hbm"]
+    out.append(dict(base, kernel="whole step", ms=line["ms_per_step"],
+                    params_per_s=line["value"], alg_gbs=h["alg_gbs"], frac_of_peak=h["alg_frac"],
+                    min_moved_gbs=h["min_moved_gbs"],
+                    oracle_s_per_step=(span_params / cpu["value"]) if cpu else None,
+                    oracle_cores=cpu.get("cores")))
+    g = line.get("gather")
+    if g:
+        r = g["roofline"]
+        out.append(dict(base, kernel="gather", ms=g["ms_per_call"], params_per_s=g["value"],
+                        alg_gbs=r["achieved"], frac_of_peak=r["frac"],
+                        moved_bytes_per_launch=r.get("traffic")))
+    return out
+
+
 def run_reference(args, w):
     rank = env_int("RANK", 0)
     if rank != 0:
@@ -460,6 +502,11 @@ def run_reference(args, w):
     if not args.no_gather and args.cpu_seconds > 0:
         g = gather_cpu_rate(w, min(args.cpu_seconds, 6.0))
         line["gather"] = {"value": g["value"], "unit": g["unit"], "cpu_baseline": g}
+    if args.results:
+        append_results(args.results, [{
+            "workload": w.name, "impl": "reference", "n_gpus": args.gpus,
+            "kernel": "whole step", "ms": line["ms_per_step"], "params_per_s": value,
+            "oracle_cores": used, "sample": sample}])
     print(json.dumps(line))
     return 0
 
@@ -720,6 +767,13 @@ def run_ours(args, w0):
         "clocks": clk,
         "last_step": {k: info[k] for k in ("step", "skipped", "global_norm", "clip_coef")},
     }
+    if args.results:
+        # the stored captures are of HBM-resident state; graph replays carry no per-kernel
+        # events, so they give the step and gather records only
+        traffic_of = ((lambda name: load_traffic(name, w)) if args.state != "host"
+                      else (lambda name: None))
+        append_results(args.results, kernel_records(line, kinds if graphs is None else {},
+                                                    kms, klaunch, w, traffic_of))
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
@@ -823,9 +877,10 @@ def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world
     return {"value": rates[best], "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": STEP_INFO_D2H_BYTES * world, "steps": steps, "mode": best,
             "by_mode": rates,
-            "host_buffers": (f"{len(gsets[0])} distinct pinned gradient buffers" if distinct == len(gsets[0])
-                             else f"{distinct} distinct pinned buffers for {len(gsets[0])} ranks, reused "
-                                  f"cyclically (this process's share of host memory)"),
+            "host_buffers": (
+                f"{len(gsets[0])} distinct pinned gradient buffers" if distinct == len(gsets[0])
+                else f"{distinct} distinct pinned buffers for {len(gsets[0])} ranks, reused "
+                     f"cyclically (this process's share of host memory)"),
             "result_read_back": ("the step info (overflow flag, skip, norm, step counter) "
                                  "each step; the fp16 parameters stay in HBM, where the "
                                  "forward pass and the gather read them"),
@@ -997,6 +1052,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU oracle baseline budget (0 skips it)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--results", default=None, metavar="PATH",
+                    help="append one JSON record per kernel (and the step and gather) to "
+                         "this file, as JSON lines")
     ap.add_argument("--no-gather", action="store_true",
                     help="step: leave out the gather and the step + gather pass")
     ap.add_argument("--state", default="device", choices=["device", "host"],

@@ -48,9 +48,14 @@ def test_default_workload_is_the_largest_single_gpu_config():
     assert bench.DEFAULT_WORKLOAD == "zero3_13b_rank0_nd64"
 
 
-def test_reference_arm_line():
+def test_reference_arm_line(tmp_path):
+    log = tmp_path / "results.jsonl"
     d = run(["--impl", "reference", "--workload", "zero2_tiny_1m_nd4", "--steps", "2",
-             "--warmup", "3", "--cpu-seconds", "0.5"])
+             "--warmup", "3", "--cpu-seconds", "0.5", "--results", str(log)])
+    recs = [json.loads(l) for l in log.read_text().splitlines()]
+    assert len(recs) == 1 and recs[0]["impl"] == "reference"
+    assert recs[0]["kernel"] == "whole step"
+    assert recs[0]["params_per_s"] == d["value"] and recs[0]["oracle_cores"] >= 1
     check_common(d)
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
     check_cpu_baseline(d["cpu_baseline"])
@@ -77,9 +82,18 @@ def test_process_spans():
 
 
 @pytest.mark.gpu
-def test_step_line():
+def test_step_line(tmp_path):
+    log = tmp_path / "results.jsonl"
     d = run(["--workload", "zero2_tiny_1m_nd4", "--steps", "20", "--warmup", "3",
-             "--cpu-seconds", "1"])
+             "--cpu-seconds", "1", "--results", str(log)])
+    # the results log: one record per kernel that ran (the one-launch step here), the
+    # whole step and the gather
+    recs = {r["kernel"]: r for r in map(json.loads, log.read_text().splitlines())}
+    assert set(recs) == {"whole step", "gather", d["roofline"]["kernel"]}
+    assert recs["whole step"]["params_per_s"] == d["value"]
+    assert recs["whole step"]["oracle_s_per_step"] > 0
+    assert abs(recs[d["roofline"]["kernel"]]["frac_of_peak"] - d["roofline"]["frac"]) < 1e-9
+    assert recs["gather"]["params_per_s"] == d["gather"]["value"]
     check_common(d)
     assert d["unit"] == "params/s" and d["higher_is_better"] is True
     e = d["e2e"]
