@@ -439,7 +439,7 @@ def append_results(path, records) -> None:
             f.write(json.dumps(dict(r, time=stamp)) + "\n")
 
 
-def kernel_records(line, kinds, kms, klaunch, w, traffic_of) -> list:
+def kernel_records(line, kinds, kms, klaunch, traffic_of) -> list:
     """The results-log records of one GPU bench line: one per kernel (its algorithmic and
     moved GB/s and fraction of peak), the whole step, and the gather if it ran."""
     peak = line["roofline"]["peak"]
@@ -648,7 +648,7 @@ def run_ours(args, w0):
     total_params = job_params(w0, world)
     value = total_params / (ms_per_step / 1e3)
 
-    e2e = run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world,
+    e2e = run_e2e(args, plan, one_step, gsets, p16, stream, barrier, job_max, world,
                   total_params) if not args.no_e2e else None
 
     gather = hot = None
@@ -675,7 +675,7 @@ def run_ours(args, w0):
         gk_ms, gk_n = z.zero_profile_read(plan, reset=True)
         if z.zero_gather_status(plan) != 0:
             raise SystemExit("the gather reported a device failure")
-        gather = gather_object(w0, offs, args.steps, job_max(gms) / args.steps,
+        gather = gather_object(offs, args.steps, job_max(gms) / args.steps,
                                gk_ms[z.PROF_GATHER], gk_n[z.PROF_GATHER], world,
                                traffic=load_traffic("gather", w0))
         if rank == 0 and args.cpu_seconds > 0:
@@ -773,7 +773,7 @@ def run_ours(args, w0):
         traffic_of = ((lambda name: load_traffic(name, w)) if args.state != "host"
                       else (lambda name: None))
         append_results(args.results, kernel_records(line, kinds if graphs is None else {},
-                                                    kms, klaunch, w, traffic_of))
+                                                    kms, klaunch, traffic_of))
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
@@ -793,8 +793,7 @@ def host_memory_bytes() -> int:
         return 0
 
 
-def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world,
-            total_params):
+def run_e2e(args, plan, one_step, gsets, p16, stream, barrier, job_max, world, total_params):
     """The step end to end through the public API from pinned host memory, in the ways a
     user can feed it, each timed over whole steps; every step includes the upload of its
     gradients and the read-back of its result (the step info: flag, skip, norm, counter).
@@ -889,7 +888,7 @@ def run_e2e(args, w, plan, one_step, gsets, p16, stream, barrier, job_max, world
                                     "d2h_bytes_per_step": p16_bytes + STEP_INFO_D2H_BYTES * world}}
 
 
-def gather_object(w, offs, calls, ms_per_call, kernel_ms, launches, world, traffic=None):
+def gather_object(offs, calls, ms_per_call, kernel_ms, launches, world, traffic=None):
     """The gather's figures: parameters moved per second (all processes), and its kernels'
     achieved HBM bandwidth (4 algorithmic bytes per parameter over their summed
     per-launch durations) against the measured peak."""
@@ -1008,7 +1007,7 @@ def run_gather(args, w):
     clk = clocks.stop()
     # with --prefetch consecutive layers overlap on two streams, so their per-launch
     # durations overlap too: the bandwidth is taken over whole calls instead
-    g = gather_object(w, offs, args.steps, ms,
+    g = gather_object(offs, args.steps, ms,
                       ms * args.steps if args.prefetch else kms[z.PROF_GATHER],
                       kl[z.PROF_GATHER], 1,
                       traffic=(None if args.layer_shift or args.prefetch
