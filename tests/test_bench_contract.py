@@ -42,6 +42,7 @@ def check_cpu_baseline(c):
 def check_roofline(r):
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert abs(r["frac_of_nominal"] - r["achieved"] / bench.NOMINAL_HBM_GBS) < 1e-9
 
 
 def test_default_workload_is_the_largest_single_gpu_config():
