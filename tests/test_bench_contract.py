@@ -97,6 +97,9 @@ def test_step_line(tmp_path):
     assert recs["gather"]["params_per_s"] == d["gather"]["value"]
     check_common(d)
     assert d["unit"] == "params/s" and d["higher_is_better"] is True
+    # the 1M workload is timed with an L2 flush before every step, each step between its
+    # own events: the median step is reported beside the mean
+    assert 0 < d["ms_per_step_median"] <= 2 * d["ms_per_step"]
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 2 * 1048576
     assert e["d2h_bytes_per_step"] > 0 and set(e["by_mode"]) == {"copy", "copy_overlap",
