@@ -919,7 +919,7 @@ def gather_object(offs, calls, ms_per_call, kernel_ms, launches, world, traffic=
 
 
 KERNEL_SOURCES = ("step_kernels.cu", "gather_kernel.cu", "bulk_async.h", "grid_sync.h",
-                  "internal.h")
+                  "internal.h", "bounds.h")
 
 
 def kernel_source_hash() -> str:

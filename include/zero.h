@@ -378,6 +378,26 @@ int zero_selftest_wait(uint32_t polls, int32_t* expired);
  * Errors: ZERO_EINVAL, ZERO_ECUDA. */
 int zero_selftest_grid_barrier(uint32_t polls, int32_t skip_one, int32_t* expired);
 
+/* Bounds report of a bounds-checked build (a facility for testing; the pages have no
+ * counterpart). A build compiled with ZERO_BOUNDS_CHECK tests the byte range of each
+ * global access of the kernels' main paths against the extent of the buffer it belongs
+ * to, skips an access outside it and records the first such fault on the current device.
+ * *enabled: 1 in such a build, 0 in the normal one (where *site and *offset are always 0).
+ * *site: 0, or the first faulting access site (1 contribution register loads, 2 fp32 sum
+ * stores, 3 contribution bulk loads, 4 update loads, 5 update stores, 6 the last few
+ * parameters, 7 one-launch state loads, 8 one-launch stores, 9 a gather tile, 10
+ * realigning-gather loads, 11 realigning-gather stores); *offset: its byte offset from
+ * the buffer's start. With reset != 0 the record is cleared after it is read. Synchronous
+ * in a checked build. Errors: ZERO_EINVAL (a NULL output), ZERO_ECUDA. */
+int zero_bounds_check(int32_t reset, int32_t* enabled, int32_t* site, int64_t* offset);
+
+/* Self-test of those checks (the pages have no counterpart): one kernel tests a range
+ * inside a 64-byte device buffer and one reaching past its end (bytes 80..95), accessing
+ * neither. In a bounds-checked build zero_bounds_check then reports site 11 at offset 80
+ * (unless an earlier fault is recorded); in the normal build it has no effect.
+ * Synchronises the device. Errors: ZERO_ECUDA. */
+int zero_selftest_bounds(void);
+
 /* Message of the calling thread's last error ("" if none). Valid until the thread's
  * next libzero call. */
 const char* zero_last_error(void);

@@ -4,7 +4,9 @@ Argument marshalling only: every step of the path runs in the library's CUDA ker
 Functions carry the C names; they accept torch tensors (their ``data_ptr()`` is passed)
 or raw integer addresses, and raise :class:`ZeroError` on a non-zero return code.
 The first call loads ``libzero.so`` and raises if it has not been built
-(``python -m sharded_emulated_reduce_gb300.build``); there is no fallback.
+(``python -m sharded_emulated_reduce_gb300.build``); there is no fallback. The environment
+variable ZERO_LIBZERO names another build of the library to load instead (the
+bounds-checked ``libzero_checked.so`` in tests).
 """
 from __future__ import annotations
 
@@ -13,7 +15,7 @@ import os
 from typing import Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libzero.so")
+LIB_PATH = os.environ.get("ZERO_LIBZERO") or os.path.join(_HERE, "libzero.so")
 
 ZERO_OK = 0
 ZERO_EINVAL = -1
@@ -102,6 +104,9 @@ _SIGS = {
     "zero_plan_set_state": ([_P, ctypes.POINTER(zero_plan_state)], ctypes.c_int),
     "zero_selftest_wait": ([ctypes.c_uint32, ctypes.POINTER(_I32)], ctypes.c_int),
     "zero_selftest_grid_barrier": ([ctypes.c_uint32, _I32, ctypes.POINTER(_I32)], ctypes.c_int),
+    "zero_bounds_check": ([_I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32),
+                           ctypes.POINTER(_I64)], ctypes.c_int),
+    "zero_selftest_bounds": ([], ctypes.c_int),
     "zero_last_error": ([], ctypes.c_char_p),
 }
 _lib_handle = None
@@ -498,6 +503,20 @@ def zero_selftest_wait(polls: int = 4096) -> int:
     out = _I32()
     _check(_lib.zero_selftest_wait(polls, ctypes.byref(out)))
     return out.value
+
+
+def zero_bounds_check(reset: bool = False) -> dict:
+    """The bounds report of a bounds-checked build: {"enabled", "site", "offset"}; site 0
+    means no access fell outside its buffer (always 0 in the normal build)."""
+    en, site, off = _I32(), _I32(), _I64()
+    _check(_lib.zero_bounds_check(1 if reset else 0, ctypes.byref(en), ctypes.byref(site),
+                                  ctypes.byref(off)))
+    return {"enabled": en.value, "site": site.value, "offset": off.value}
+
+
+def zero_selftest_bounds() -> None:
+    """Run the bounds self-test (see zero.h): a checked build then reports site 11."""
+    _check(_lib.zero_selftest_bounds())
 
 
 def zero_selftest_grid_barrier(polls: int = 4096, skip_one: bool = True) -> int:

@@ -17,6 +17,7 @@
 // blocks (funnel shifts) into aligned 16-byte stores to global memory.
 #include <atomic>
 
+#include "bounds.h"
 #include "bulk_async.h"
 #include "internal.h"
 
@@ -58,6 +59,11 @@ __device__ __forceinline__ AlTile al_tile(const GatherLaunch& a, int& seg, long 
   m.head = (long long)(((16u - (unsigned)(da & 15u)) & 15u) >> 1);
   if (m.head > m.n) m.head = m.n;
   m.body = ((sa + 2 * m.head) & 15u) ? 0 : ((m.n - m.head) >> 3) << 3;
+  // the tile's source and destination lie inside its segment (every copy of the tile,
+  // bulk or element by element, is inside the tile)
+  if (!ZERO_IN_BOUNDS(kSiteGatherTile, m.src, 2 * (size_t)m.n, sg.src, 2 * (size_t)sg.len) ||
+      !ZERO_IN_BOUNDS(kSiteGatherTile, m.dst, 2 * (size_t)m.n, sg.dst, 2 * (size_t)sg.len))
+    m.n = m.head = m.body = 0;
   return m;
 }
 
@@ -136,6 +142,11 @@ __device__ __forceinline__ MisTile mis_tile(const GatherLaunch& L, int& seg, lon
   m.v1 = m.head + 8 * m.j_hi;
   if (m.v0 > m.n) m.v0 = m.n;
   if (m.v1 > m.n) m.v1 = m.n;
+  // the tile's source and destination lie inside its segment
+  if (!ZERO_IN_BOUNDS(kSiteGatherTile, m.src, 2 * (size_t)m.n, sg.src, 2 * (size_t)sg.len) ||
+      !ZERO_IN_BOUNDS(kSiteGatherTile, m.dst, 2 * (size_t)m.n, sg.dst, 2 * (size_t)sg.len)) {
+    m.n = m.head = m.j_lo = m.j_hi = m.v0 = m.v1 = 0;
+  }
   return m;
 }
 
@@ -301,6 +312,8 @@ __global__ void __launch_bounds__(kMisThreads, 1)
     const unsigned char* src;
     uint32_t bytes;
     if (!next_stretch(L, prod, &src, &bytes)) return;
+    const GatherSeg& sg = L.seg[prod.seg];
+    if (!ZERO_IN_BOUNDS(kSiteRealignLoad, src, bytes, sg.src, 2 * (size_t)sg.len)) return;
     const int s = (int)(issued % kMisStages);
     mbar_expect_tx(&full[s], bytes);
     bulk_load(smem + (size_t)s * kMisStageBytes, src, bytes, &full[s]);
@@ -325,7 +338,8 @@ __global__ void __launch_bounds__(kMisThreads, 1)
       if (nv > kMisVecs) nv = kMisVecs;
       const int s = (int)(q % kMisStages);
       bool landed = mbar_wait(&full[s], (uint32_t)((q / kMisStages) & 1));
-      if (landed) {
+      if (landed && ZERO_IN_BOUNDS(kSiteRealignStore, out + jb, 16 * (size_t)nv, L.seg[seg].dst,
+                                   2 * (size_t)L.seg[seg].len)) {
         const uint4* w = reinterpret_cast<const uint4*>(smem + (size_t)s * kMisStageBytes);
         switch (m.d) {  // even byte offsets 2..14 (0 only in tiles without vectors)
           case 0: realign_stretch<0, kMisThreads>(w, out + jb, nv); break;
@@ -402,6 +416,40 @@ cudaError_t launch_gather(const GatherLaunch& p, cudaStream_t s) {
   const int grid = p.grid > 0 ? p.grid : gather_grid(p.tiles);
   k_gather<<<grid, kGatThreads, kGatSmem, s>>>(p);
   return cudaGetLastError();
+}
+
+namespace {
+// 64 bytes that the bounds self-test measures ranges against (never read or written)
+__device__ uint16_t g_bounds_probe_buf[32];
+
+// The bounds self-test: one range inside g_bounds_probe_buf and one reaching past its end
+// (bytes 80..95 of a 64-byte buffer) are tested; neither is accessed.
+__global__ void k_bounds_probe() {
+  if (threadIdx.x != 0) return;
+  const uint16_t* b = g_bounds_probe_buf;
+  bool inside = ZERO_IN_BOUNDS(kSiteGatherTile, b + 8, 16, b, 64);
+  bool outside = ZERO_IN_BOUNDS(kSiteRealignStore, b + 40, 16, b, 64);
+  (void)inside;
+  (void)outside;
+}
+}  // namespace
+
+cudaError_t bounds_probe() {
+  k_bounds_probe<<<1, 32>>>();
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : cudaDeviceSynchronize();
+}
+
+// This translation unit's bounds-fault words (see bounds.h): 0 and the words in a checked
+// build, 1 (and zeros) in the normal one, -1 on a CUDA error.
+int bounds_words_gather(unsigned long long* out, bool reset) {
+#ifdef ZERO_BOUNDS_CHECK
+  return bounds_fault_words(out, reset);
+#else
+  (void)reset;
+  out[0] = out[1] = 0;
+  return 1;
+#endif
 }
 
 }  // namespace zero

@@ -146,6 +146,14 @@ cudaError_t launch_small_step(const SmallLaunch& p, cudaStream_t s);
 constexpr int32_t kStatusStepWait = 5;  // the fused step's grid barrier expired
 cudaError_t launch_gather(const GatherLaunch& p, cudaStream_t s);
 
+// The bounds-fault words {site, offset} of the step and gather kernels' translation units
+// (bounds.h): return 0 in a bounds-checked build, 1 (zeros written) in the normal build,
+// -1 on a CUDA error; `reset` zeroes them after the read.
+int bounds_words_step(unsigned long long* out, bool reset);
+int bounds_words_gather(unsigned long long* out, bool reset);
+// Runs the bounds self-test kernel (gather_kernel.cu) and waits for it.
+cudaError_t bounds_probe();
+
 // Set the calling thread's zero_last_error() message; returns code.
 int set_error(int code, const char* msg);
 

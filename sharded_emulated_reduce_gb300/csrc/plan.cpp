@@ -719,6 +719,27 @@ int zero_memory_bytes(int64_t n, int32_t nd, int32_t align, int32_t stage, int64
   return ZERO_OK;
 }
 
+int zero_bounds_check(int32_t reset, int32_t* enabled, int32_t* site, int64_t* offset) {
+  g_error.clear();
+  if (!enabled || !site || !offset) return fail(ZERO_EINVAL, "enabled, site and offset are required");
+  unsigned long long a[2], b[2];
+  const int ra = zero::bounds_words_step(a, reset != 0);
+  const int rb = zero::bounds_words_gather(b, reset != 0);
+  if (ra < 0 || rb < 0) return fail(ZERO_ECUDA, "reading the bounds-fault words failed");
+  const unsigned long long* f = a[0] != 0 ? a : b;
+  *enabled = ra == 0 ? 1 : 0;
+  *site = static_cast<int32_t>(f[0]);
+  *offset = static_cast<int64_t>(f[1]);
+  return ZERO_OK;
+}
+
+int zero_selftest_bounds(void) {
+  g_error.clear();
+  const cudaError_t e = zero::bounds_probe();
+  if (e != cudaSuccess) return cuda_fail(e, "bounds self-test");
+  return ZERO_OK;
+}
+
 int zero_profile_enable(zero_plan* p, int32_t on) {
   g_error.clear();
   if (!p) return fail(ZERO_EINVAL, "plan is NULL");

@@ -32,6 +32,7 @@
 
 #include <atomic>
 
+#include "bounds.h"
 #include "bulk_async.h"
 #include "grid_sync.h"
 #include "internal.h"
@@ -342,12 +343,31 @@ struct ReduceArgs {
 // compile time; ND == 0 reads it from the arguments. Up to 8 ranks all loads are issued
 // at once; beyond that they are issued 8 ranks at a time, which keeps the register count
 // (and so the number of resident warps) at the level that saturates HBM.
+// Group v (8 elements, 16 bytes) of rank r's contribution, streamed (evict-first).
+template <int CAP>
+__device__ __forceinline__ uint4 load_contribution(const ReduceArgs<CAP>& a, int r, long long v) {
+  const uint4* p = reinterpret_cast<const uint4*>(a.g[r]) + v;
+  if (!ZERO_IN_BOUNDS(kSiteReduceLoad, p, 16, a.g[r], (size_t)a.n_vec * 16))
+    return make_uint4(0u, 0u, 0u, 0u);
+  return __ldcs(p);
+}
+
+// Group v's fp32 sums into the workspace.
+template <int CAP>
+__device__ __forceinline__ void store_sums(const ReduceArgs<CAP>& a, long long v,
+                                           const float (&s)[8]) {
+  float4* o = reinterpret_cast<float4*>(a.gsum) + 2 * v;
+  if (!ZERO_IN_BOUNDS(kSiteReduceStore, o, 32, a.gsum, (size_t)a.n_vec * 32)) return;
+  o[0] = make_float4(s[0], s[1], s[2], s[3]);
+  o[1] = make_float4(s[4], s[5], s[6], s[7]);
+}
+
 template <int ND, int CAP>
 __device__ __forceinline__ void sum_group(const ReduceArgs<CAP>& a, long long v, float (&s)[8]) {
   if constexpr (ND > 0 && ND <= 8) {
     uint4 w[ND];
 #pragma unroll
-    for (int r = 0; r < ND; ++r) w[r] = __ldcs(reinterpret_cast<const uint4*>(a.g[r]) + v);
+    for (int r = 0; r < ND; ++r) w[r] = load_contribution(a, r, v);
 #pragma unroll
     for (int r = 0; r < ND; ++r) add_vec(s, w[r]);
   } else {
@@ -357,7 +377,7 @@ __device__ __forceinline__ void sum_group(const ReduceArgs<CAP>& a, long long v,
       uint4 w[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (r0 + j < nd) w[j] = __ldcs(reinterpret_cast<const uint4*>(a.g[r0 + j]) + v);
+        if (r0 + j < nd) w[j] = load_contribution(a, r0 + j, v);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (r0 + j < nd) add_vec(s, w[j]);
@@ -404,9 +424,7 @@ __global__ void __launch_bounds__(kThreads, (ND >= 32) ? 5 : 0)
         add_square(acc, fin ? s[j] : 0.0f);
       }
     }
-    float4* o = reinterpret_cast<float4*>(a.gsum) + 2 * v;
-    o[0] = make_float4(s[0], s[1], s[2], s[3]);
-    o[1] = make_float4(s[4], s[5], s[6], s[7]);
+    store_sums(a, v, s);
   }
 
   // CTA partial, then the last CTA to arrive combines all partials (no waiting).
@@ -594,10 +612,13 @@ __global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
           s_chunk[s] = k;
           mbar_expect_tx(&full[s], bytes * (uint32_t)nr);
           unsigned char* dst = smem + (size_t)s * kRbStageBytes;
-          for (int j = 0; j < nr; ++j)
-            bulk_load(dst + (size_t)j * TG * 16,
-                      reinterpret_cast<const unsigned char*>(a.g[r0 + j]) + v0 * 16, bytes,
-                      &full[s]);
+          for (int j = 0; j < nr; ++j) {
+            const unsigned char* src =
+                reinterpret_cast<const unsigned char*>(a.g[r0 + j]) + v0 * 16;
+            if (ZERO_IN_BOUNDS(kSiteBulkReduceLoad, src, bytes, a.g[r0 + j],
+                               (size_t)a.n_vec * 16))
+              bulk_load(dst + (size_t)j * TG * 16, src, bytes, &full[s]);
+          }
           ++q;
         }
         if (!ok) break;
@@ -673,9 +694,7 @@ __global__ void __launch_bounds__(RbCfg<CONS>::kThreads, 1)
           bad += fin ? 0 : 1;
           add_square(acc, fin ? s[j][e] : 0.0f);
         }
-        float4* o = reinterpret_cast<float4*>(a.gsum) + 2 * v;
-        o[0] = make_float4(s[j][0], s[j][1], s[j][2], s[j][3]);
-        o[1] = make_float4(s[j][4], s[j][5], s[j][6], s[j][7]);
+        store_sums(a, v, s[j]);
       }
     }
   }
@@ -833,10 +852,15 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
     const uint32_t bytes = (uint32_t)(tile_len(t) * sizeof(float));
     float* d = in + (size_t)s * 4 * kUpdTile;
     mbar_expect_tx(&full[s], 4 * bytes);
-    bulk_load(d, a.gsum + base, bytes, &full[s]);
-    bulk_load(d + kUpdTile, a.master + base, bytes, &full[s]);
-    bulk_load(d + 2 * kUpdTile, a.m + base, bytes, &full[s]);
-    bulk_load(d + 3 * kUpdTile, a.v + base, bytes, &full[s]);
+    const size_t ext = (size_t)a.n_valid * sizeof(float);
+    if (ZERO_IN_BOUNDS(kSiteUpdateLoad, a.gsum + base, bytes, a.gsum, ext))
+      bulk_load(d, a.gsum + base, bytes, &full[s]);
+    if (ZERO_IN_BOUNDS(kSiteUpdateLoad, a.master + base, bytes, a.master, ext))
+      bulk_load(d + kUpdTile, a.master + base, bytes, &full[s]);
+    if (ZERO_IN_BOUNDS(kSiteUpdateLoad, a.m + base, bytes, a.m, ext))
+      bulk_load(d + 2 * kUpdTile, a.m + base, bytes, &full[s]);
+    if (ZERO_IN_BOUNDS(kSiteUpdateLoad, a.v + base, bytes, a.v, ext))
+      bulk_load(d + 3 * kUpdTile, a.v + base, bytes, &full[s]);
   };
 
   if (tid == 0) {
@@ -886,10 +910,17 @@ __global__ void __launch_bounds__(kUpdThreads, 1) k_update(const __grid_constant
     if (tid == 0) {
       const float* o = outf + (size_t)ob * 3 * kUpdTile;
       const uint32_t bytes = (uint32_t)(cnt * sizeof(float));
-      bulk_store(a.master + base, o, bytes);
-      bulk_store(a.m + base, o + kUpdTile, bytes);
-      bulk_store(a.v + base, o + 2 * kUpdTile, bytes);
-      bulk_store(a.p16 + base, outh + (size_t)ob * kUpdTile, (uint32_t)(cnt * sizeof(uint16_t)));
+      const size_t ext = (size_t)a.n_valid * sizeof(float);
+      const uint32_t hbytes = (uint32_t)(cnt * sizeof(uint16_t));
+      if (ZERO_IN_BOUNDS(kSiteUpdateStore, a.master + base, bytes, a.master, ext))
+        bulk_store(a.master + base, o, bytes);
+      if (ZERO_IN_BOUNDS(kSiteUpdateStore, a.m + base, bytes, a.m, ext))
+        bulk_store(a.m + base, o + kUpdTile, bytes);
+      if (ZERO_IN_BOUNDS(kSiteUpdateStore, a.v + base, bytes, a.v, ext))
+        bulk_store(a.v + base, o + 2 * kUpdTile, bytes);
+      if (ZERO_IN_BOUNDS(kSiteUpdateStore, a.p16 + base, hbytes, a.p16,
+                         (size_t)a.n_valid * sizeof(uint16_t)))
+        bulk_store(a.p16 + base, outh + (size_t)ob * kUpdTile, hbytes);
       bulk_commit();
       if (tile_of(k + kUpdStages) < ntiles) issue(k + kUpdStages, s);
     }
@@ -1096,9 +1127,13 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   auto issue_state_loads = [&]() {
     if (tid == 0 && state_bytes > 0) {
       mbar_expect_tx(state_bar, 3 * state_bytes);
-      bulk_load(s_master, a.master + e0, state_bytes, state_bar);
-      bulk_load(s_m, a.m + e0, state_bytes, state_bar);
-      bulk_load(s_v, a.v + e0, state_bytes, state_bar);
+      const size_t ext = (size_t)a.r.n_valid * sizeof(float);
+      if (ZERO_IN_BOUNDS(kSiteSmallState, a.master + e0, state_bytes, a.master, ext))
+        bulk_load(s_master, a.master + e0, state_bytes, state_bar);
+      if (ZERO_IN_BOUNDS(kSiteSmallState, a.m + e0, state_bytes, a.m, ext))
+        bulk_load(s_m, a.m + e0, state_bytes, state_bar);
+      if (ZERO_IN_BOUNDS(kSiteSmallState, a.v + e0, state_bytes, a.v, ext))
+        bulk_load(s_v, a.v + e0, state_bytes, state_bar);
     }
   };
 
@@ -1208,6 +1243,10 @@ __global__ void __launch_bounds__(kSmallThreads + 32, 1)
   auto update = [&](auto load_state) {
     for (long long q = tid; q < nq; q += kSmallThreads) {
       const long long i = e0 + 4 * q;
+      // master, m, v and the fp16 parameters share the index: one range test covers them
+      if (!ZERO_IN_BOUNDS(kSiteSmallStore, master + i, 16, master,
+                          (size_t)a.r.n_valid * sizeof(float)))
+        continue;
       const float4 g = g4[q];
       float4 p, m, v;
       load_state(q, i, p, m, v);
@@ -1512,6 +1551,18 @@ cudaError_t launch_update(const UpdateLaunch& p, cudaStream_t s) {
   if (p.grid > 0 && p.grid < grid) grid = p.grid;
   k_update<<<(int)grid, kUpdThreads, kUpdSmem, s>>>(a);
   return cudaGetLastError();
+}
+
+// This translation unit's bounds-fault words (see bounds.h): 0 and the words in a checked
+// build, 1 (and zeros) in the normal one, -1 on a CUDA error.
+int bounds_words_step(unsigned long long* out, bool reset) {
+#ifdef ZERO_BOUNDS_CHECK
+  return bounds_fault_words(out, reset);
+#else
+  (void)reset;
+  out[0] = out[1] = 0;
+  return 1;
+#endif
 }
 
 }  // namespace zero

@@ -1,3 +1,4 @@
+import ctypes
 """The C ABI of libzero without a GPU: it loads, exports every symbol include/zero.h
 declares, computes the partition and accounting like the oracle, and rejects every bad
 argument with the right code before any CUDA call."""
@@ -177,6 +178,15 @@ def test_selftest_rejects_bad_poll_counts():
     for polls in (0, 2**24 + 1):
         expect(z.ZERO_EINVAL, z.zero_selftest_wait, polls)
         expect(z.ZERO_EINVAL, z.zero_selftest_grid_barrier, polls)
+
+
+def test_bounds_report_of_the_normal_build():
+    # the normal build compiles no checks: it reports them off, with no fault, and needs
+    # no device to say so; NULL outputs are rejected
+    assert z.zero_bounds_check() == {"enabled": 0, "site": 0, "offset": 0}
+    lib = z.lib()
+    out = z._I32()
+    assert lib.zero_bounds_check(0, None, ctypes.byref(out), None) == z.ZERO_EINVAL
 
 
 def test_gather_status_without_a_gather_is_zero():
