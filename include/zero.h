@@ -175,7 +175,7 @@ int zero_plan_bind(zero_plan* plan, int32_t r0, int32_t r1, float* master, float
  * most 3072 groups of 8 parameters per SM (and nd <= 64) runs as one cooperative launch
  * that keeps the fp32 sums in shared memory; other spans run a reduce and an update
  * kernel. When the span
- * fills at least one wave of the reduce, a one-thread kernel computing the next step's
+ * fills at least one wave of the reduce, a one-warp kernel computing the next step's
  * step-counter-only scalars runs on a second stream that the plan owns, forked from
  * `stream` after the reduce and joined back into it after the update (stream order for
  * the caller is unchanged). The launches contain no host-side decision, so the call can
