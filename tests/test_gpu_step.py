@@ -43,6 +43,19 @@ def test_odd_shapes_and_rank_counts(n, nd):
     assert r.exact
 
 
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 5, 7, 8, 9, 16, 24, 32, 33, 63, 64, 65, 128])
+def test_two_kernel_path_every_reduce_variant(nd):
+    # spans above the one-launch limit (3072 groups of 8 per SM): every branch of the
+    # reduce's dispatch, the register-load reduce for fewer than 8 ranks (counts fixed at
+    # compile time or read at run time) and the bulk-load reduce from 8 ranks on (fixed
+    # counts 8, 16, 32, 64 and run-time counts up to 64 and beyond), then the update, over
+    # two steps with a ragged tail
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 8 * 3072 * sms + 37  # just past the one-launch limit, not a multiple of 8
+    r = Runner(small(n=n, nd=nd, r1=nd, cfg=700 + nd), mode="full_parallel").run()
+    assert r.exact
+
+
 @pytest.mark.parametrize("align", [8, 16, 128])
 @pytest.mark.parametrize("r0,r1", [(0, 1), (1, 3), (2, 3), (0, 3)])
 def test_rank_subranges_and_alignment(align, r0, r1):
